@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Throughput of the gated sparse attention decode step at 128K context.
+
+One step = one sparse_attn_decode call for a batch of 32 sequences, each with
+131072 cached rows: indexer scan over every cached indexer key, exact Top-K
+(K=2048), gathered attention over the kept rows with the sigmoid gate, split-K
+combine. Prints one JSON line (rank 0). Also reports, in the same line, the
+prefill throughput of the 8K workload, the dominant kernel's roofline, an
+end-to-end number through host buffers, and the fp64 oracle timed on the host.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own batch of 32 sequences (weak scaling, no
+collective on the data path; the only collectives are the timing barrier and
+the max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode tok/s @128K ctx K=2048; prefill tok/s; % of roofline"
+WORKLOAD = "decode_128k"
+PREFILL_WORKLOAD = "prefill_8k"
+SCAN_KERNEL_SRC = os.path.join(ROOT, "indexer_top_sparse_03_b300", "csrc", "decode_scan.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# process group helpers (also exercised by the gloo tests on CPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[int(str(device).split(":")[1])])
+        else:
+            dist.barrier()
+
+
+def aggregate_throughput(units_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job units per second: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML, read-only)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    REASONS = {0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle",
+               0x2: "applications_clocks_setting", 0x10: "sync_boost", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.handle = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM)
+        except Exception:                                   # no NVML: report nothing
+            self.nvml = None
+
+    def _run(self):
+        nv = self.nvml
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.handle, nv.NVML_CLOCK_SM))
+                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+                for b, name in self.REASONS.items():
+                    if bits & b:
+                        self.reasons.add(name)
+            except Exception:
+                break
+            time.sleep(0.0005)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def file_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, src: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's source
+    is unchanged since the capture."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE)).get(kernel)
+    if not d or d.get("source_sha") != file_sha(src):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def decode_bytes(cfg, lens):
+    """Algorithmic bytes of one decode step and of its indexer scan."""
+    n = sum(lens)
+    scan = n * cfg.di * 2 + cfg.B * cfg.Hi * (cfg.di * 2 + 4)
+    kept = sum(min(cfg.K, x) for x in lens)
+    row = (cfg.dqk * 2 + cfg.dv * 2) if not cfg.latent else cfg.dqk * 2
+    gather = kept * row
+    small = cfg.B * (cfg.Hq * cfg.dqk * 2 + cfg.Hq * 4 + cfg.Hq * cfg.dv * 2 + 12)
+    return scan + gather + small, scan
+
+
+def oracle_sample_decode(cfg, seed, nseq, nthreads=0):
+    """Time the fp64 oracle on nseq sequences of the workload (CPU)."""
+    import oracle
+    from workloads import get_config, make_decode
+    small = get_config(cfg.name, B=nseq)
+    inp = make_decode(small, seed=seed)
+    t0 = time.perf_counter()
+    oracle.decode_layer(inp, small.K, small.dv, 1 / math.sqrt(small.dqk), nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, oracle.threads_used(nthreads, nseq)
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from workloads import get_config
+    cfg = get_config(WORKLOAD)
+    ncores = os.cpu_count() or 1
+    nseq = max(1, min(cfg.B, ncores))
+    times = []
+    cores = 1
+    for i in range(args.warmup + args.steps):
+        dt, cores = oracle_sample_decode(cfg, args.seed + i, nseq)
+        if i >= args.warmup:
+            times.append(dt)
+    step = sum(times) / len(times)
+    value = nseq / step
+    sample = (f"{nseq} of the {cfg.B} sequences of one decode step (ctx {cfg.ctx}, K {cfg.K}) "
+              f"per step, full layer in fp64")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(cfg),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg):
+    return {"workload": cfg.name, "batch_per_gpu": cfg.B, "ctx": cfg.ctx, "K": cfg.K, "Hq": cfg.Hq,
+            "dqk": cfg.dqk, "dv": cfg.dv, "Hi": cfg.Hi, "di": cfg.di, "attn_dtype": "bf16",
+            "indexer_dtype": "bf16",
+            "l2": "inputs larger than L2: every step streams the 537 MB indexer-key cache",
+            "parallelism": "replicas, one batch per GPU, no data-path collective"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def bench_prefill(sa, torch, dev, seed, iters=10):
+    """Prefill tok/s of the 8K workload, plus the standalone indexer's tensor rate."""
+    from workloads import get_config, make_prefill
+    cfg = get_config(PREFILL_WORKLOAD)
+    inp = make_prefill(cfg, seed=seed, device=dev)
+    scale = 1 / math.sqrt(cfg.dqk)
+    out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((cfg.L, cfg.K), dtype=torch.int32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record()
+        sa.sparse_attn_prefill(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], inp["w"],
+                               inp["gate"], cfg.K, scale, out=out, idx_out=idx,
+                               stage_events=None if e is None else e[1:])
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    for i in range(iters):
+        step(ev[i])
+    torch.cuda.synchronize()
+    tot = [ev[i][0].elapsed_time(ev[i][2]) for i in range(iters)]
+    sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(iters)]
+    ms = statistics.median(tot)
+    # standalone indexer (all causal rows), for its tensor-core rate
+    scores = torch.empty((cfg.L, cfg.L), dtype=torch.float32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        sa.indexer_score(inp["q_idx"], inp["w"], inp["k_idx"], scores=scores)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(iters):
+        sa.indexer_score(inp["q_idx"], inp["w"], inp["k_idx"], scores=scores)
+    e1.record()
+    torch.cuda.synchronize()
+    ix_ms = e0.elapsed_time(e1) / iters
+    pairs = cfg.L * (cfg.L + 1) // 2
+    flops = 2 * cfg.Hi * cfg.di * pairs
+    peaks = measured_peaks()
+    ix_tflops = flops / (ix_ms * 1e-3) / 1e12
+    del scores
+    return {"workload": cfg.name, "L": cfg.L, "K": cfg.K, "tok_s": cfg.L / (ms * 1e-3), "ms": ms,
+            "selection_ms": statistics.median(sel), "attention_ms": ms - statistics.median(sel),
+            "indexer_ms": ix_ms, "indexer_tflops": ix_tflops,
+            "indexer_frac_of_bf16_peak": ix_tflops / peaks["bf16_tflops"],
+            "indexer_peak_source": peaks["source"] + " burst bf16"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import indexer_top_sparse_03_b300 as sa
+    from indexer_top_sparse_03_b300.binding import DecodeArgs  # noqa: F401
+    from workloads import get_config, make_decode
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    sa.load_library()
+
+    cfg = get_config(WORKLOAD)
+    inp = make_decode(cfg, seed=args.seed + rank, device=dev)
+    lens = inp["lens"]
+    scale = 1 / math.sqrt(cfg.dqk)
+    out = torch.empty((cfg.B, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=dev)
+    max_ctx = max(lens)
+
+    def step(events=None):
+        sa.sparse_attn_decode(inp["q"], inp["q_idx"], inp["w"], inp["gate"], inp["k_cache"],
+                              inp["v_cache"], inp["k_idx_cache"], inp["seq_start"], inp["ctx_len"],
+                              max_ctx, cfg.K, scale, out=out, idx_out=idx, stage_events=events)
+
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e in ev:                     # create the events before the timed region
+        for x in e:
+            x.record()
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dev)
+    torch.cuda.synchronize()
+    with clocks:
+        t_start.record()
+        for i in range(K):
+            ev[i][0].record()
+            step(ev[i][1:])
+        t_end.record()
+        torch.cuda.synchronize()
+    barrier(dev)
+    ms_step = t_start.elapsed_time(t_end) / K
+    ms_step_max = reduce_max(ms_step, dev)
+    value = aggregate_throughput(cfg.B, world, ms_step_max * 1e-3)
+    stage = {
+        "indexer_scan_ms": statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)),
+        "topk_ms": statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)),
+        "attention_ms": statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(K)),
+    }
+    step_bytes, scan_bytes = decode_bytes(cfg, lens)
+    peaks = measured_peaks()
+    scan_s = stage["indexer_scan_ms"] * 1e-3
+    achieved = scan_bytes / scan_s / 1e9
+    traffic = recorded_traffic("decode_scan_kernel", SCAN_KERNEL_SRC)
+    roofline = {"kernel": "decode_scan_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": peaks["source"], "algorithmic_bytes": scan_bytes,
+                "traffic": traffic,
+                "step_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+    # end to end through host buffers: per step copy q, q_idx, w, gate in from
+    # pinned memory, run the step, copy the output back, wait for it
+    host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_idx", "w", "gate")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for k_, t in host.items():
+            inp[k_].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+    for _ in range(W):
+        e2e_step()
+    barrier(dev)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_s = reduce_max((time.perf_counter() - t0) / K, dev)
+    e2e = {"value": aggregate_throughput(cfg.B, world, e2e_s), "unit": "tok/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    prefill = None
+    if not args.no_prefill:
+        del host
+        prefill = bench_prefill(sa, torch, dev, args.seed + rank)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ncores = os.cpu_count() or 1
+        nseq = max(1, min(cfg.B, ncores))
+        dt, cores = oracle_sample_decode(cfg, args.seed, nseq)
+        cpu = {"value": nseq / dt, "unit": "tok/s", "cores": cores, "kind": "oracle",
+               "sample": f"{nseq} of the {cfg.B} sequences of one decode step (ctx {cfg.ctx}, "
+                         f"K {cfg.K}), full layer in fp64 ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
+                "warmup": W, "ms_per_step": ms_step_max, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(cfg), "roofline": roofline, "stages_ms": stage,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K,
+                "clocks": clocks.summary(), "prefill": prefill}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=int(os.environ.get("WORLD_SIZE", "1")))
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,288 @@
+// C ABI of the sparse attention library: argument checks, workspace layout and
+// the order of the launches. Every check runs on the host before anything is
+// enqueued; nothing here allocates device memory or synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "../../include/sparse_attn.h"
+
+namespace sa {
+bool attention_mma_supported(const AttnArgs& a);
+}
+
+namespace {
+
+constexpr size_t WS_ALIGN = 256;
+constexpr int MAX_K = 65536;
+
+size_t align_up(size_t x) { return (x + WS_ALIGN - 1) / WS_ALIGN * WS_ALIGN; }
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+bool valid_dtype(int d) { return d == SA_F32 || d == SA_BF16 || d == SA_FP8_E4M3; }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_LAUNCH; }
+
+int check_indexer_shape(int dtype, int Hi, int di)
+{
+    if (!valid_dtype(dtype)) return SA_ERR_INVALID_ARG;
+    if (Hi < 1 || di < 1) return SA_ERR_INVALID_ARG;
+    if (Hi > 32 || di % 16 != 0 || di > 256) return SA_ERR_UNSUPPORTED;
+    return SA_OK;
+}
+
+// ---- prefill workspace layout --------------------------------------------
+struct PrefillLayout {
+    int64_t rows_per_pass;   // query rows scored per indexer/Top-K pass
+    size_t idx_off, scores_off, total;
+};
+
+PrefillLayout prefill_layout(const sa_prefill_args& a)
+{
+    PrefillLayout l{};
+    const int64_t L = a.L;
+    const int64_t budget = int64_t(1) << 30;               // bytes of scores per pass
+    int64_t rows = budget / (4 * (L > 0 ? L : 1));
+    rows = rows < 1 ? 1 : (rows > L ? L : rows);
+    l.rows_per_pass = rows;
+    size_t off = 0;
+    l.idx_off = off;
+    if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * (size_t)L * a.K);
+    l.scores_off = off;
+    off += align_up(sizeof(float) * (size_t)rows * (size_t)L);
+    l.total = off;
+    return l;
+}
+
+int check_prefill_scalars(const sa_prefill_args* a)
+{
+    if (!a) return SA_ERR_INVALID_ARG;
+    if (a->L < 0 || a->Hq < 1 || a->dqk < 1 || a->dv < 1 || a->K < 1) return SA_ERR_INVALID_ARG;
+    int st = check_indexer_shape(a->idx_dtype, a->Hi, a->di);
+    if (st != SA_OK) return st;
+    if (a->attn_dtype != SA_F32 && a->attn_dtype != SA_BF16) {
+        return a->attn_dtype == SA_FP8_E4M3 ? SA_ERR_UNSUPPORTED : SA_ERR_INVALID_ARG;
+    }
+    if (a->ld_k < a->dqk || a->ld_v < a->dv) return SA_ERR_INVALID_ARG;
+    if (a->K > MAX_K || a->Hq > 64) return SA_ERR_UNSUPPORTED;
+    if (a->dqk % 8 != 0 || a->dv % 8 != 0 || a->ld_k % 8 != 0 || a->ld_v % 8 != 0) return SA_ERR_UNSUPPORTED;
+    if (a->attn_dtype == SA_BF16 ? (a->dqk > 576 || a->dv > 512) : (a->dqk > 256 || a->dv > 512))
+        return SA_ERR_UNSUPPORTED;
+    if (!(a->softmax_scale == a->softmax_scale)) return SA_ERR_INVALID_ARG;   // NaN
+    return SA_OK;
+}
+
+int check_prefill(const sa_prefill_args* a)
+{
+    int st = check_prefill_scalars(a);
+    if (st != SA_OK || a->L == 0) return st;
+    if (!a->q || !a->k || !a->v || !a->q_idx || !a->k_idx || !a->w || !a->gate || !a->out)
+        return SA_ERR_INVALID_ARG;
+    if (a->idx_dtype == SA_FP8_E4M3 && (!a->q_scale || !a->k_scale)) return SA_ERR_INVALID_ARG;
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->q_idx, 16) ||
+        !aligned(a->k_idx, 16) || !aligned(a->out, 16) || !aligned(a->w, 4) || !aligned(a->gate, 4))
+        return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+// ---- decode workspace layout ----------------------------------------------
+struct DecodeLayout {
+    int splits;
+    size_t scores_off, idx_off, part_off, tickets_off, total;
+};
+
+DecodeLayout decode_layout(const sa_decode_args& a)
+{
+    DecodeLayout l{};
+    l.splits = sa::attention_splits(a.K, a.max_ctx, a.B);
+    size_t off = 0;
+    l.scores_off = off;
+    off += align_up(sizeof(float) * (size_t)a.B * (size_t)(a.max_ctx > 0 ? a.max_ctx : 1));
+    l.idx_off = off;
+    if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * (size_t)a.B * a.K);
+    l.part_off = off;
+    if (l.splits > 1) off += align_up(sizeof(float) * (size_t)a.B * l.splits * a.Hq * (a.dv + 2));
+    l.tickets_off = off;
+    off += align_up(sizeof(unsigned) * (size_t)a.B * a.Hq);
+    l.total = off;
+    return l;
+}
+
+int check_decode_scalars(const sa_decode_args* a)
+{
+    if (!a) return SA_ERR_INVALID_ARG;
+    if (a->B < 0 || a->Hq < 1 || a->dqk < 1 || a->dv < 1 || a->K < 1 || a->max_ctx < 0)
+        return SA_ERR_INVALID_ARG;
+    if (!valid_dtype(a->idx_dtype) || !valid_dtype(a->attn_dtype)) return SA_ERR_INVALID_ARG;
+    if (a->Hi < 1 || a->di < 1) return SA_ERR_INVALID_ARG;
+    if (a->ld_k < a->dqk || a->ld_v < a->dv) return SA_ERR_INVALID_ARG;
+    if (a->attn_dtype != SA_BF16 || a->idx_dtype != SA_BF16) return SA_ERR_UNSUPPORTED;
+    if (a->Hi > 32 || a->di % 32 != 0 || a->di > 256) return SA_ERR_UNSUPPORTED;
+    if (a->dqk % 16 != 0 || a->dv % 16 != 0 || a->dqk > 576 || a->dv > 512) return SA_ERR_UNSUPPORTED;
+    if (a->ld_k % 8 != 0 || a->ld_v % 8 != 0 || a->K > MAX_K || a->Hq > 64) return SA_ERR_UNSUPPORTED;
+    if (a->max_ctx >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+    if (!(a->softmax_scale == a->softmax_scale)) return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+int check_decode(const sa_decode_args* a)
+{
+    int st = check_decode_scalars(a);
+    if (st != SA_OK || a->B == 0) return st;
+    if (!a->q || !a->q_idx || !a->w || !a->gate || !a->k_cache || !a->v_cache || !a->k_idx_cache ||
+        !a->seq_start || !a->ctx_len || !a->out)
+        return SA_ERR_INVALID_ARG;
+    if (!aligned(a->q, 16) || !aligned(a->q_idx, 16) || !aligned(a->k_cache, 16) ||
+        !aligned(a->v_cache, 16) || !aligned(a->k_idx_cache, 16) || !aligned(a->out, 16) ||
+        !aligned(a->seq_start, 8) || !aligned(a->ctx_len, 4))
+        return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sa_status_string(int status)
+{
+    switch (status) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument";
+    case SA_ERR_UNSUPPORTED: return "unsupported dtype or shape";
+    case SA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SA_ERR_LAUNCH: return "CUDA launch error";
+    default: return "unknown status";
+    }
+}
+
+int sa_version(void) { return 100; }
+
+int indexer_score(const void* q_idx, int dtype, const float* q_scale, const float* w,
+                  const void* k_idx, const float* k_scale, int T, int N, int Hi, int di,
+                  int64_t causal_offset, float* scores, int64_t ld_s, cudaStream_t stream)
+{
+    if (T < 0 || N < 0) return SA_ERR_INVALID_ARG;
+    int st = check_indexer_shape(dtype, Hi, di);
+    if (st != SA_OK) return st;
+    if (T == 0 || N == 0) return SA_OK;
+    if (!q_idx || !w || !k_idx || !scores || ld_s < N) return SA_ERR_INVALID_ARG;
+    if (dtype == SA_FP8_E4M3 && (!q_scale || !k_scale)) return SA_ERR_INVALID_ARG;
+    if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(scores, 4) || !aligned(w, 4))
+        return SA_ERR_INVALID_ARG;
+    sa::IndexerArgs a{};
+    a.q_idx = q_idx; a.dtype = dtype; a.q_scale = q_scale; a.w = w;
+    a.k_idx = k_idx; a.k_scale = k_scale;
+    a.T = T; a.N = N; a.Hi = Hi; a.di = di; a.causal_offset = causal_offset;
+    a.t_begin = 0; a.scores = scores; a.ld_s = ld_s;
+    return status_of(sa::launch_indexer(a, stream));
+}
+
+int topk_select(const float* scores, int64_t ld_s, const int32_t* row_len, int T, int K,
+                int32_t* idx_out, cudaStream_t stream)
+{
+    if (T < 0 || K < 1 || ld_s < 1) return SA_ERR_INVALID_ARG;
+    if (K > MAX_K) return SA_ERR_UNSUPPORTED;
+    if (T == 0) return SA_OK;
+    if (!scores || !row_len || !idx_out) return SA_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || !aligned(row_len, 4) || !aligned(idx_out, 4)) return SA_ERR_INVALID_ARG;
+    sa::TopkArgs a{};
+    a.scores = scores; a.ld_s = ld_s; a.row_len = row_len; a.causal_first = 0;
+    a.n_cap = ld_s; a.rows = T; a.K = K; a.idx = idx_out; a.ld_idx = K;
+    return status_of(sa::launch_topk(a, stream));
+}
+
+size_t sa_prefill_workspace_size(const sa_prefill_args* args)
+{
+    if (check_prefill_scalars(args) != SA_OK) return 0;
+    return prefill_layout(*args).total;
+}
+
+int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    int st = check_prefill(args);
+    if (st != SA_OK) return st;
+    const sa_prefill_args& a = *args;
+    if (a.L == 0) return SA_OK;
+    const PrefillLayout lay = prefill_layout(a);
+    if (!ws || ws_bytes < lay.total || !aligned(ws, WS_ALIGN)) return SA_ERR_WORKSPACE;
+    char* wsb = static_cast<char*>(ws);
+    int32_t* idx = a.idx_out ? a.idx_out : reinterpret_cast<int32_t*>(wsb + lay.idx_off);
+    float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
+
+    for (int64_t t0 = 0; t0 < a.L; t0 += lay.rows_per_pass) {
+        const int64_t t1 = (t0 + lay.rows_per_pass < a.L) ? t0 + lay.rows_per_pass : a.L;
+        sa::IndexerArgs ia{};
+        ia.q_idx = a.q_idx; ia.dtype = a.idx_dtype; ia.q_scale = a.q_scale; ia.w = a.w;
+        ia.k_idx = a.k_idx; ia.k_scale = a.k_scale;
+        ia.T = (int)t1; ia.N = (int)t1; ia.Hi = a.Hi; ia.di = a.di; ia.causal_offset = 0;
+        ia.t_begin = (int)t0; ia.scores = scores; ia.ld_s = a.L;
+        cudaError_t e = sa::launch_indexer(ia, stream);
+        if (e != cudaSuccess) return SA_ERR_LAUNCH;
+        sa::TopkArgs ta{};
+        ta.scores = scores; ta.ld_s = a.L; ta.row_len = nullptr; ta.causal_first = t0;
+        ta.n_cap = a.L; ta.rows = (int)(t1 - t0); ta.K = a.K; ta.idx = idx + t0 * a.K; ta.ld_idx = a.K;
+        e = sa::launch_topk(ta, stream);
+        if (e != cudaSuccess) return SA_ERR_LAUNCH;
+    }
+    if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    sa::AttnArgs at{};
+    at.q = a.q; at.k = a.k; at.ld_k = a.ld_k; at.v = a.v; at.ld_v = a.ld_v;
+    at.v_aliases_k = (a.v == a.k) && a.ld_v == a.ld_k;
+    at.row_base = nullptr; at.idx = idx; at.K = a.K; at.ctx_len = nullptr;
+    at.causal_first = 0; at.n_cap = a.L; at.gate = a.gate;
+    at.rows = a.L; at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
+    at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype; at.out = a.out;
+    at.splits = 1; at.part = nullptr; at.tickets = nullptr;
+    if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (a.stage_events && cudaEventRecord(a.stage_events[1], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    return SA_OK;
+}
+
+size_t sa_decode_workspace_size(const sa_decode_args* args)
+{
+    if (check_decode_scalars(args) != SA_OK) return 0;
+    return decode_layout(*args).total;
+}
+
+int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    int st = check_decode(args);
+    if (st != SA_OK) return st;
+    const sa_decode_args& a = *args;
+    if (a.B == 0) return SA_OK;
+    const DecodeLayout lay = decode_layout(a);
+    if (!ws || ws_bytes < lay.total || !aligned(ws, WS_ALIGN)) return SA_ERR_WORKSPACE;
+    char* wsb = static_cast<char*>(ws);
+    float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
+    int32_t* idx = a.idx_out ? a.idx_out : reinterpret_cast<int32_t*>(wsb + lay.idx_off);
+    float* part = reinterpret_cast<float*>(wsb + lay.part_off);
+    unsigned* tickets = reinterpret_cast<unsigned*>(wsb + lay.tickets_off);
+
+    if (cudaMemsetAsync(tickets, 0, sizeof(unsigned) * (size_t)a.B * a.Hq, stream) != cudaSuccess)
+        return SA_ERR_LAUNCH;
+    sa::DecodeScanArgs da{};
+    da.q_idx = a.q_idx; da.w = a.w; da.k_idx = a.k_idx_cache; da.seq_start = a.seq_start;
+    da.ctx_len = a.ctx_len; da.max_ctx = a.max_ctx; da.B = a.B; da.Hi = a.Hi; da.di = a.di;
+    da.scores = scores; da.tickets = tickets;
+    if (sa::launch_decode_scan(da, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+
+    sa::TopkArgs ta{};
+    ta.scores = scores; ta.ld_s = a.max_ctx > 0 ? a.max_ctx : 1; ta.row_len = a.ctx_len;
+    ta.causal_first = 0; ta.n_cap = a.max_ctx; ta.rows = a.B; ta.K = a.K; ta.idx = idx; ta.ld_idx = a.K;
+    if (sa::launch_topk(ta, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (a.stage_events && cudaEventRecord(a.stage_events[1], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+
+    sa::AttnArgs at{};
+    at.q = a.q; at.k = a.k_cache; at.ld_k = a.ld_k; at.v = a.v_cache; at.ld_v = a.ld_v;
+    at.v_aliases_k = (a.v_cache == a.k_cache) && a.ld_v == a.ld_k;
+    at.row_base = a.seq_start; at.idx = idx; at.K = a.K; at.ctx_len = a.ctx_len;
+    at.causal_first = 0; at.n_cap = a.max_ctx; at.gate = a.gate;
+    at.rows = a.B; at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
+    at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype; at.out = a.out;
+    at.splits = lay.splits; at.part = part; at.tickets = tickets;
+    if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (a.stage_events && cudaEventRecord(a.stage_events[2], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    return SA_OK;
+}
+
+}  // extern "C"

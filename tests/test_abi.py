@@ -1,0 +1,180 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, its argument structures match the ctypes mirrors, and argument
+errors come back as status codes before anything is enqueued."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from indexer_top_sparse_03_b300 import binding
+from indexer_top_sparse_03_b300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sparse_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*SA_API\s+(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(binding.EXPORTS) <= set(names), names
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    assert "workspace" in binding.status_string(binding.SA_ERR_WORKSPACE)
+    assert binding.status_string(12345) == "unknown status"
+    assert lib.sa_version() >= 100
+
+
+def _c_offsets(struct, fields, tmp_path):
+    src = tmp_path / "off.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){",
+             f'printf("%zu\\n", sizeof({struct}));']
+    lines += [f'printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    lines.append("return 0;}")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "off"
+    subprocess.check_call(["gcc", "-I/usr/local/cuda/include", "-o", str(exe), str(src)])
+    return [int(x) for x in subprocess.check_output([str(exe)]).split()]
+
+
+@pytest.mark.parametrize("struct,mirror", [("sa_prefill_args", binding.PrefillArgs),
+                                           ("sa_decode_args", binding.DecodeArgs)])
+def test_argument_structs_match_header(struct, mirror, tmp_path):
+    fields = [f for f, _ in mirror._fields_]
+    got = _c_offsets(struct, fields, tmp_path)
+    assert got[0] == ctypes.sizeof(mirror)
+    assert got[1:] == [getattr(mirror, f).offset for f in fields]
+
+
+def _prefill(**kw):
+    a = binding.PrefillArgs()
+    a.L, a.Hq, a.dqk, a.dv, a.Hi, a.di, a.K = 128, 16, 128, 128, 4, 64, 32
+    a.softmax_scale, a.attn_dtype, a.idx_dtype = 0.1, binding.SA_BF16, binding.SA_BF16
+    a.ld_k, a.ld_v = 128, 128
+    fake = 1 << 20                       # never dereferenced: every call here fails first
+    for f in ("q", "k", "v", "q_idx", "k_idx", "w", "gate", "out"):
+        setattr(a, f, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _decode(**kw):
+    a = binding.DecodeArgs()
+    a.B, a.Hq, a.dqk, a.dv, a.Hi, a.di, a.K = 4, 16, 128, 128, 4, 64, 2048
+    a.softmax_scale, a.attn_dtype, a.idx_dtype = 0.1, binding.SA_BF16, binding.SA_BF16
+    a.ld_k, a.ld_v, a.max_ctx = 128, 128, 131072
+    fake = 1 << 20
+    for f in ("q", "q_idx", "w", "gate", "k_cache", "v_cache", "k_idx_cache", "seq_start",
+              "ctx_len", "out"):
+        setattr(a, f, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_workspace_sizes(lib):
+    a = _prefill()
+    n = lib.sa_prefill_workspace_size(ctypes.byref(a))
+    assert n >= 4 * 128 * 32 + 4 * 128 * 128 and n % 256 == 0
+    a.idx_out = 1 << 20
+    assert lib.sa_prefill_workspace_size(ctypes.byref(a)) < n
+    d = _decode()
+    m = lib.sa_decode_workspace_size(ctypes.byref(d))
+    assert m >= 4 * 4 * 131072 and m % 256 == 0
+    assert lib.sa_prefill_workspace_size(ctypes.byref(_prefill(K=0))) == 0
+    assert lib.sa_prefill_workspace_size(None) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=0), binding.SA_ERR_INVALID_ARG),
+    (dict(K=70000), binding.SA_ERR_UNSUPPORTED),
+    (dict(Hq=0), binding.SA_ERR_INVALID_ARG),
+    (dict(idx_dtype=7), binding.SA_ERR_INVALID_ARG),
+    (dict(attn_dtype=binding.SA_FP8_E4M3), binding.SA_ERR_UNSUPPORTED),
+    (dict(Hi=33), binding.SA_ERR_UNSUPPORTED),
+    (dict(di=40), binding.SA_ERR_UNSUPPORTED),
+    (dict(ld_k=64), binding.SA_ERR_INVALID_ARG),
+    (dict(q=None), binding.SA_ERR_INVALID_ARG),
+    (dict(q=(1 << 20) + 4), binding.SA_ERR_INVALID_ARG),
+    (dict(idx_dtype=binding.SA_FP8_E4M3), binding.SA_ERR_INVALID_ARG),   # scales missing
+    (dict(softmax_scale=float("nan")), binding.SA_ERR_INVALID_ARG),
+])
+def test_prefill_argument_errors(lib, kw, status):
+    a = _prefill(**kw)
+    assert lib.sparse_attn_prefill(ctypes.byref(a), 1 << 30, 1 << 30, None) == status
+
+
+def test_prefill_workspace_errors(lib):
+    a = _prefill()
+    need = lib.sa_prefill_workspace_size(ctypes.byref(a))
+    assert lib.sparse_attn_prefill(ctypes.byref(a), None, need, None) == binding.SA_ERR_WORKSPACE
+    assert lib.sparse_attn_prefill(ctypes.byref(a), 1 << 30, need - 1, None) == binding.SA_ERR_WORKSPACE
+    assert lib.sparse_attn_prefill(ctypes.byref(a), (1 << 30) + 16, need, None) == binding.SA_ERR_WORKSPACE
+    assert lib.sparse_attn_prefill(None, 1 << 30, need, None) == binding.SA_ERR_INVALID_ARG
+
+
+def test_empty_inputs_are_no_ops(lib):
+    assert lib.sparse_attn_prefill(ctypes.byref(_prefill(L=0)), None, 0, None) == 0
+    assert lib.sparse_attn_decode(ctypes.byref(_decode(B=0)), None, 0, None) == 0
+    assert lib.indexer_score(None, 1, None, None, None, None, 0, 5, 4, 64, 0, None, 5, None) == 0
+    assert lib.topk_select(None, 5, None, 0, 3, None, None) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=0), binding.SA_ERR_INVALID_ARG),
+    (dict(max_ctx=-1), binding.SA_ERR_INVALID_ARG),
+    (dict(max_ctx=1 << 31), binding.SA_ERR_UNSUPPORTED),
+    (dict(idx_dtype=binding.SA_FP8_E4M3), binding.SA_ERR_UNSUPPORTED),
+    (dict(attn_dtype=binding.SA_F32), binding.SA_ERR_UNSUPPORTED),
+    (dict(di=48), binding.SA_ERR_UNSUPPORTED),
+    (dict(ctx_len=None), binding.SA_ERR_INVALID_ARG),
+    (dict(seq_start=(1 << 20) + 4), binding.SA_ERR_INVALID_ARG),
+])
+def test_decode_argument_errors(lib, kw, status):
+    a = _decode(**kw)
+    assert lib.sparse_attn_decode(ctypes.byref(a), 1 << 30, 1 << 40, None) == status
+
+
+def test_decode_workspace_errors(lib):
+    a = _decode()
+    need = lib.sa_decode_workspace_size(ctypes.byref(a))
+    assert lib.sparse_attn_decode(ctypes.byref(a), 1 << 30, need - 256, None) == binding.SA_ERR_WORKSPACE
+
+
+def test_standalone_argument_errors(lib):
+    f = 1 << 20
+    assert lib.indexer_score(f, 1, None, f, f, None, 8, 8, 0, 64, 0, f, 8, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.indexer_score(f, 1, None, f, f, None, 8, 8, 4, 64, 0, f, 7, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.indexer_score(f, 2, None, f, f, None, 8, 8, 4, 64, 0, f, 8, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.indexer_score(f, 1, None, f, f, None, -1, 8, 4, 64, 0, f, 8, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.topk_select(f, 8, f, 4, 0, f, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.topk_select(f, 8, None, 4, 2, f, None) == binding.SA_ERR_INVALID_ARG
+    assert lib.topk_select(f, 8, f, 4, 1 << 20, f, None) == binding.SA_ERR_UNSUPPORTED
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.load_library(str(tmp_path / "nope.so"))

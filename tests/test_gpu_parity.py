@@ -1,0 +1,237 @@
+"""CUDA library vs the fp64 oracle, through the C ABI, at sizes the oracle
+finishes in seconds (several tiles, ragged tails), plus edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import (RTOL_SCORE, check_kept_set, check_outputs, check_scores, score_denominators,
+                    to_host)
+from workloads import get_config, make_decode, make_prefill, quantize_rows_e4m3
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def sa(cuda_ok):
+    import indexer_top_sparse_03_b300 as pkg
+    from indexer_top_sparse_03_b300.build import build
+    build()
+    pkg.load_library()
+    return pkg
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def _indexer_inputs(T, N, Hi, di, dtype, seed):
+    g = _gen(seed)
+    qf = torch.randn((T, Hi, di), generator=g)
+    kf = torch.randn((N, di), generator=g)
+    w = torch.softmax(torch.randn((T, Hi), generator=g), -1)
+    if dtype == torch.float8_e4m3fn:
+        q, qs = quantize_rows_e4m3(qf)
+        k, ks = quantize_rows_e4m3(kf)
+        return q, qs, w, k, ks
+    return qf.to(dtype), None, w, kf.to(dtype), None
+
+
+# ---------------------------------------------------------------------------
+# indexer_score
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float8_e4m3fn])
+@pytest.mark.parametrize("Hi,di", [(1, 16), (4, 32), (4, 64), (8, 64), (32, 128), (3, 48)])
+def test_indexer_score(sa, dtype, Hi, di):
+    T, N = 203, 389
+    q, qs, w, k, ks = _indexer_inputs(T, N, Hi, di, dtype, seed=Hi * 1000 + di)
+    dq = lambda x: None if x is None else x.to(DEV)
+    for off in (0, 186, -7, N):
+        got = sa.indexer_score(dq(q), dq(w), dq(k), dq(qs), dq(ks), causal_offset=off)
+        got = to_host(got).double().numpy()
+        rows = np.arange(T)
+        n = np.clip(rows + 1 + off, 0, N)
+        ref = oracle.indexer(q, w, k, rows, np.zeros(T), n, qs, ks)
+        den = score_denominators(q, w, k, rows, np.zeros(T), n, qs, ks)
+        for t in range(T):
+            check_scores(got[t, :n[t]], ref[t], den[t], RTOL_SCORE[dtype], f"off={off} t={t}")
+            assert np.isnan(got[t, n[t]:]).all(), "positions beyond n_t must stay unwritten"
+
+
+def test_indexer_all_negative_dots_give_exact_zero(sa):
+    T, N, Hi, di = 40, 70, 4, 64
+    g = _gen(1)
+    k = torch.randn((N, di), generator=g).abs().to(torch.bfloat16)
+    q = (-torch.rand((T, Hi, di), generator=g)).to(torch.bfloat16)
+    w = torch.softmax(torch.randn((T, Hi), generator=g), -1)
+    got = to_host(sa.indexer_score(q.to(DEV), w.to(DEV), k.to(DEV), causal_offset=N))
+    assert (got == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# topk_select: bit-exact against the oracle's sort on the same fp32 values
+# ---------------------------------------------------------------------------
+
+def _topk_case(sa, rows, K, ld=None):
+    n = [len(r) for r in rows]
+    ld = ld or max(max(n), 1)
+    buf = torch.full((len(rows), ld), float("nan"), dtype=torch.float32)
+    for i, r in enumerate(rows):
+        buf[i, :len(r)] = torch.as_tensor(r, dtype=torch.float32)
+    lens = torch.tensor(n, dtype=torch.int32)
+    got = to_host(sa.topk_select(buf.to(DEV), lens.to(DEV), K)).numpy()
+    ref = oracle.topk([buf[i, :n[i]].double().numpy() for i in range(len(rows))], K)
+    for i in range(len(rows)):
+        m = min(K, n[i])
+        assert np.array_equal(got[i, :m], np.sort(ref[i, :m])), f"row {i} (n={n[i]})"
+        assert (got[i, m:] == -1).all()
+
+
+@pytest.mark.parametrize("K", [1, 7, 64, 2048])
+def test_topk_random_rows(sa, K):
+    rng = np.random.default_rng(K)
+    lens = [0, 1, K - 1 if K > 1 else 0, K, K + 1, 3 * K + 5, 12000, 12289, 40000]
+    rows = [rng.standard_normal(n).astype(np.float32) for n in lens]
+    _topk_case(sa, rows, K)
+
+
+def test_topk_heavy_ties_signed_zeros_and_negatives(sa):
+    rng = np.random.default_rng(5)
+    K = 100
+    rows = [rng.integers(-2, 3, size=5000).astype(np.float32),       # few distinct values
+            np.zeros(300, np.float32),                                # all equal
+            np.where(rng.random(700) < 0.5, -0.0, 0.0).astype(np.float32),
+            -np.abs(rng.standard_normal(900)).astype(np.float32),     # all negative
+            np.repeat(rng.standard_normal(10), 50).astype(np.float32),
+            np.concatenate([np.full(20000, 1.5), np.full(20000, 2.5)]).astype(np.float32)]
+    _topk_case(sa, rows, K)
+
+
+def test_topk_long_rows_from_global_memory(sa):
+    rng = np.random.default_rng(9)
+    rows = [rng.standard_normal(n).astype(np.float32) * 3 for n in (131072, 200001)]
+    _topk_case(sa, rows, 2048)
+
+
+def test_topk_row_len_clamped_to_stride(sa):
+    buf = torch.arange(10, dtype=torch.float32).reshape(1, 10).to(DEV)
+    lens = torch.tensor([50], dtype=torch.int32, device=DEV)      # clamped to ld_s = 10
+    got = to_host(sa.topk_select(buf, lens, 3)).numpy()
+    assert got.tolist() == [[7, 8, 9]]
+
+
+# ---------------------------------------------------------------------------
+# prefill: all rows at small sizes
+# ---------------------------------------------------------------------------
+
+def _run_prefill(sa, cfg, inp):
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    idx = torch.empty((cfg.L, cfg.K), dtype=torch.int32, device=DEV)
+    out = sa.sparse_attn_prefill(d["q"], d["k"], d["v"], d["q_idx"], d["k_idx"], d["w"], d["gate"],
+                                 cfg.K, 1 / math.sqrt(cfg.dqk), q_scale=d["q_scale"],
+                                 k_scale=d["k_scale"], idx_out=idx)
+    torch.cuda.synchronize()
+    return to_host(out), to_host(idx).numpy()
+
+
+def _check_prefill_rows(cfg, inp, out, idx, rows):
+    rows = np.asarray(rows)
+    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows),
+                                rows + 1, inp["q_scale"], inp["k_scale"])
+    for i, t in enumerate(rows):
+        check_kept_set(idx[t], ref_scores[i], cfg.K, f"row {t}")
+    ref = oracle.attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], cfg.dv, inp["gate"],
+                        rows, np.zeros_like(rows), idx[rows], 1 / math.sqrt(cfg.dqk))
+    check_outputs(out[rows].double().numpy(), ref, cfg.attn_dtype, "prefill out")
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),
+    ("prefill_8k", dict(L=1500, K=256)),
+    ("prefill_128k", dict(L=1300, K=200)),
+    ("prefill_8k", dict(L=700, K=1024)),          # K >= n for every row: full causal attention
+])
+def test_prefill_parity(sa, name, over):
+    cfg = get_config(name, **over)
+    inp = make_prefill(cfg, seed=11)
+    out, idx = _run_prefill(sa, cfg, inp)
+    _check_prefill_rows(cfg, inp, out, idx, np.arange(cfg.L))
+
+
+def test_prefill_latent_row(sa):
+    # one 576-wide row per token, values are its first 512 columns
+    cfg = get_config("prefill_8k", L=300, K=64, dqk=576, dv=512, qkv_std=1 / 24)
+    inp = make_prefill(cfg, seed=12)
+    kv = inp["k"]
+    inp = dict(inp, v=kv, ld_v=576)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    idx = torch.empty((cfg.L, cfg.K), dtype=torch.int32, device=DEV)
+    out = sa.sparse_attn_prefill(d["q"], d["k"], d["k"], d["q_idx"], d["k_idx"], d["w"], d["gate"],
+                                 cfg.K, 1 / math.sqrt(576), dv=512, idx_out=idx)
+    torch.cuda.synchronize()
+    _check_prefill_rows(cfg, inp, to_host(out), to_host(idx).numpy(), np.arange(cfg.L))
+
+
+def test_prefill_zero_indexer_keeps_lowest_positions(sa):
+    cfg = get_config("prefill_8k", L=400, K=32)
+    inp = make_prefill(cfg, seed=13)
+    inp["q_idx"] = torch.zeros_like(inp["q_idx"])          # every score is exactly 0
+    out, idx = _run_prefill(sa, cfg, inp)
+    for t in range(cfg.L):
+        m = min(cfg.K, t + 1)
+        assert idx[t, :m].tolist() == list(range(m))
+    _check_prefill_rows(cfg, inp, out, idx, np.arange(0, cfg.L, 7))
+
+
+# ---------------------------------------------------------------------------
+# decode: all sequences at small sizes
+# ---------------------------------------------------------------------------
+
+def _run_decode(sa, cfg, inp):
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=DEV)
+    out = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"],
+                                d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]),
+                                cfg.K, 1 / math.sqrt(cfg.dqk), dv=cfg.dv, ld_k=inp["ld_k"],
+                                ld_v=inp["ld_v"], idx_out=idx)
+    torch.cuda.synchronize()
+    return to_host(out), to_host(idx).numpy()
+
+
+def _check_decode(cfg, inp, out, idx, seqs=None):
+    seqs = np.arange(cfg.B) if seqs is None else np.asarray(seqs)
+    lens = np.asarray(inp["lens"])
+    starts = inp["seq_start"].numpy()
+    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx_cache"], seqs, starts[seqs],
+                                lens[seqs], inp["q_scale"], inp["k_idx_scale"])
+    for i, b in enumerate(seqs):
+        check_kept_set(idx[b], ref_scores[i], cfg.K, f"seq {b}")
+    ref = oracle.attend(inp["q"], inp["k_cache"], inp["v_cache"], inp["ld_k"], inp["ld_v"], cfg.dv,
+                        inp["gate"], seqs, starts[seqs], idx[seqs], 1 / math.sqrt(cfg.dqk))
+    check_outputs(out[seqs].double().numpy(), ref, cfg.attn_dtype, "decode out")
+
+
+@pytest.mark.parametrize("name,over", [
+    ("decode_ragged", dict(B=8, ctx_range=(), ctx_list=(1, 100, 2047, 2048, 2049, 4097, 9000, 0))),
+    ("decode_mla", dict(B=5, ctx=6000)),
+    ("decode_128k", dict(B=3, ctx=20000, K=512)),
+])
+def test_decode_parity(sa, name, over):
+    cfg = get_config(name, **over)
+    inp = make_decode(cfg, seed=21)
+    out, idx = _run_decode(sa, cfg, inp)
+    _check_decode(cfg, inp, out, idx)
+
+
+def test_decode_repeated_calls_reuse_workspace(sa):
+    cfg = get_config("decode_ragged", B=4, ctx_range=(), ctx_list=(3000, 5000, 2500, 4100))
+    inp = make_decode(cfg, seed=22)
+    a_out, a_idx = _run_decode(sa, cfg, inp)
+    b_out, b_idx = _run_decode(sa, cfg, inp)
+    assert np.array_equal(a_idx, b_idx)
+    assert torch.equal(a_out, b_out)
