@@ -105,10 +105,11 @@ attn_mma_kernel(AttnArgs a)
     const int dqk = a.dqk, dv = a.dv;
     const int qs_ld = dqk + PAD, ks_ld = dqk + PAD, vs_ld = dv + PAD, ps_ld = CHUNK + PAD;
 
+    const int stages = a.stages;
     bf16* Qs = reinterpret_cast<bf16*>(smem_raw);
     bf16* Ks = Qs + 16 * qs_ld;
-    bf16* Vs = Ks + 2 * CHUNK * ks_ld;
-    bf16* Ps = Vs + (a.v_aliases_k ? 0 : 2 * CHUNK * vs_ld);
+    bf16* Vs = Ks + stages * CHUNK * ks_ld;
+    bf16* Ps = Vs + (a.v_aliases_k ? 0 : stages * CHUNK * vs_ld);
     const int vld = a.v_aliases_k ? ks_ld : vs_ld;
 
     const int64_t n = attn_hist_len(a, r);
@@ -169,10 +170,10 @@ attn_mma_kernel(AttnArgs a)
 
     if (nchunks > 0) issue(0, 0);
     for (int c = 0; c < nchunks; ++c) {
-        const int buf = c & 1;
+        const int buf = stages == 2 ? (c & 1) : 0;
         cp_async_wait<0>();
         __syncthreads();
-        if (c + 1 < nchunks) issue(c + 1, buf ^ 1);
+        if (stages == 2 && c + 1 < nchunks) issue(c + 1, buf ^ 1);
 
         const bf16* Kb = Ks + buf * CHUNK * ks_ld;
         const bf16* Vb = a.v_aliases_k ? Kb : Vs + buf * CHUNK * vs_ld;
@@ -249,6 +250,10 @@ attn_mma_kernel(AttnArgs a)
                 mma_16816(o[2 * np], af, bfm[0], bfm[1]);
                 mma_16816(o[2 * np + 1], af, bfm[2], bfm[3]);
             }
+        }
+        if (stages == 1 && c + 1 < nchunks) {     // single buffer: refill once everyone is done
+            __syncthreads();
+            issue(c + 1, 0);
         }
     }
 
@@ -392,14 +397,25 @@ attn_simt_kernel(AttnArgs a)
     }
 }
 
-template <int NT>
-cudaError_t launch_mma(const AttnArgs& a, cudaStream_t s)
+size_t mma_smem_bytes(const AttnArgs& a, int stages)
 {
-    const size_t smem = sizeof(bf16) * ((size_t)16 * (a.dqk + PAD) + 2 * CHUNK * (a.dqk + PAD) +
-                                         (a.v_aliases_k ? 0 : 2 * CHUNK * (a.dv + PAD)) +
-                                         16 * (CHUNK + PAD));
+    return sizeof(bf16) * ((size_t)16 * (a.dqk + PAD) + (size_t)stages * CHUNK * (a.dqk + PAD) +
+                           (a.v_aliases_k ? 0 : (size_t)stages * CHUNK * (a.dv + PAD)) +
+                           16 * (CHUNK + PAD));
+}
+
+constexpr size_t MMA_SMEM_LIMIT = 200 * 1024;    // leaves room for static shared memory
+
+template <int NT>
+cudaError_t launch_mma(AttnArgs a, cudaStream_t s)
+{
+    a.stages = mma_smem_bytes(a, 2) <= MMA_SMEM_LIMIT ? 2 : 1;
+    const size_t smem = mma_smem_bytes(a, a.stages);
     cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();                  // do not leave the error latched
+        return e;
+    }
     dim3 grid(a.rows, a.splits, (a.Hq + 15) / 16);
     attn_mma_kernel<NT><<<grid, AT_THREADS, smem, s>>>(a);
     return cudaGetLastError();
@@ -410,6 +426,7 @@ cudaError_t launch_mma(const AttnArgs& a, cudaStream_t s)
 bool attention_mma_supported(const AttnArgs& a)
 {
     if (a.dtype != SA_BF16) return false;
+    if (mma_smem_bytes(a, 1) > MMA_SMEM_LIMIT) return false;
     if (a.dqk % 16 != 0 || a.dqk > 576) return false;
     if (a.dv % 64 != 0 || a.dv > 512) return false;
     if (a.v_aliases_k && a.dv > a.dqk) return false;

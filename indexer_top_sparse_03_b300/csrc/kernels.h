@@ -59,6 +59,7 @@ struct AttnArgs {
     int splits;
     float* part;            // [rows, splits, Hq, dv + 2]
     unsigned* tickets;      // [rows], zero on entry, left zero on exit
+    int stages;             // set by the launcher: gather buffers (1 or 2)
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 int attention_splits(int K, int64_t n_cap, int rows);

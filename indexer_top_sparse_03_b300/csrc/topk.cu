@@ -158,7 +158,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s)
     if (a.n_cap <= SMEM_KEYS) {
         const size_t smem = sizeof(uint32_t) * (size_t)SMEM_KEYS;
         cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
         topk_rows_kernel<true><<<a.rows, TK_THREADS, smem, s>>>(a);
     } else {
         topk_rows_kernel<false><<<a.rows, TK_THREADS, 0, s>>>(a);

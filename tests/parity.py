@@ -24,7 +24,7 @@ import oracle
 RTOL_SCORE = {torch.float32: 1e-3, torch.bfloat16: 1e-3, torch.float8_e4m3fn: 5e-2}
 BOUNDARY_RTOL = 1e-3
 OUT_ATOL, OUT_RTOL = 2e-2, 1e-2
-TIGHT_ATOL, TIGHT_RTOL = {torch.float32: (1e-5, 1e-4), torch.bfloat16: (2e-3, 1.6e-2)}
+TIGHT = {torch.float32: (1e-5, 1e-4), torch.bfloat16: (2e-3, 1.6e-2)}
 
 
 def abs_codes(t):
@@ -77,7 +77,7 @@ def check_outputs(got, ref, dtype, what=""):
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - ref)
     assert (err <= OUT_ATOL + OUT_RTOL * np.abs(ref)).all(), f"{what}: outside 2e-2/1e-2"
-    ta, tr = TIGHT_ATOL[dtype]
+    ta, tr = TIGHT[dtype]
     bad = err > ta + tr * np.abs(ref)
     assert not bad.any(), f"{what}: {bad.sum()} outputs off, worst abs {err.max():.3e}"
 

@@ -194,6 +194,8 @@ def test_prefill_zero_indexer_keeps_lowest_positions(sa):
 
 def _run_decode(sa, cfg, inp):
     d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    if inp["v_cache"] is inp["k_cache"]:
+        d["v_cache"] = d["k_cache"]                        # keep the latent row aliased
     idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=DEV)
     out = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"],
                                 d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]),
@@ -235,3 +237,18 @@ def test_decode_repeated_calls_reuse_workspace(sa):
     b_out, b_idx = _run_decode(sa, cfg, inp)
     assert np.array_equal(a_idx, b_idx)
     assert torch.equal(a_out, b_out)
+
+
+def test_decode_latent_row_given_as_separate_value_copy(sa):
+    # the same numbers, but v handed over as its own buffer: the attention kernel
+    # then gathers K and V rows separately (single-buffered, 576 + 512 wide rows)
+    cfg = get_config("decode_mla", B=3, ctx=3000)
+    inp = make_decode(cfg, seed=23)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    v_copy = inp["k_cache"][:, :cfg.dv].contiguous().to(DEV)
+    idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=DEV)
+    out = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], v_copy,
+                                d["k_idx_cache"], d["seq_start"], d["ctx_len"], 3000, cfg.K,
+                                1 / math.sqrt(cfg.dqk), dv=cfg.dv, idx_out=idx)
+    torch.cuda.synchronize()
+    _check_decode(cfg, inp, to_host(out), to_host(idx).numpy())
