@@ -212,6 +212,27 @@ SA_API size_t sa_decode_workspace_size(const sa_decode_args* args);
 SA_API int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* Bytes of device scratch the library carries for sparse_attn_decode_noalloc. */
+#define SA_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * sparse_attn_decode_noalloc -- sparse_attn_decode for callers that cannot
+ * allocate device memory (plugins whose host owns every allocation, code that
+ * must not allocate once serving has started). The paper has no counterpart:
+ * this is a deployment convenience, not part of the layer.
+ *
+ * Same arguments, kernels and results as sparse_attn_decode, but the scratch
+ * lives in a fixed array of SA_DECODE_NOALLOC_SCRATCH_BYTES inside the
+ * library, held on every GPU that loads the library until the process exits.
+ * Calls whose sa_decode_workspace_size(args) exceeds that size return
+ * SA_ERR_WORKSPACE and enqueue nothing. Nothing is allocated. All calls share
+ * the array, which keeps the previous call's contents (the step clears what
+ * must start at zero); calls whose GPU work overlaps (other streams or host
+ * threads) race and give wrong results. The first call on each device looks
+ * up the array's device address; make it before any stream capture begins.
+ */
+SA_API int sparse_attn_decode_noalloc(const sa_decode_args* args, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ SA_F32, SA_BF16, SA_FP8_E4M3 = 0, 1, 2
 
 EXPORTS = ("sa_status_string", "sa_version", "indexer_score", "topk_select",
            "sa_prefill_workspace_size", "sparse_attn_prefill",
-           "sa_decode_workspace_size", "sparse_attn_decode")
+           "sa_decode_workspace_size", "sparse_attn_decode", "sparse_attn_decode_noalloc")
 
 _P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 
@@ -78,6 +78,8 @@ def load_library(path: str | None = None):
     lib.sa_decode_workspace_size.restype = _SZ
     lib.sparse_attn_decode.argtypes = [ctypes.POINTER(DecodeArgs), _P, _SZ, _P]
     lib.sparse_attn_decode.restype = _I
+    lib.sparse_attn_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), _P]
+    lib.sparse_attn_decode_noalloc.restype = _I
     if path is None:
         _lib = lib
     return lib
@@ -258,4 +260,22 @@ def sparse_attn_decode(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_sta
     st = lib.sparse_attn_decode(ctypes.byref(a), _ptr(ws), ws.numel() * ws.element_size(),
                                 _stream(q.device, stream))
     _check("sparse_attn_decode", st)
+    return out
+
+
+def sparse_attn_decode_noalloc(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len,
+                               max_ctx: int, K: int, softmax_scale: float, dv=None, q_scale=None,
+                               k_idx_scale=None, ld_k=None, ld_v=None, out=None, idx_out=None,
+                               stream=None):
+    """sparse_attn_decode without a workspace, for callers that cannot allocate: the
+    library's own fixed scratch array is used (see include/sparse_attn.h). Only
+    `out`/`idx_out` are allocated here, and only when not given."""
+    B, Hq, dqk = q.shape
+    dv = (v_cache.shape[-1] if v_cache is not k_cache else dqk) if dv is None else dv
+    if out is None:
+        out = torch.empty((B, Hq, dv), dtype=q.dtype, device=q.device)
+    a = decode_args(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len, max_ctx,
+                    K, softmax_scale, dv, out, q_scale, k_idx_scale, ld_k, ld_v, idx_out)
+    st = load_library().sparse_attn_decode_noalloc(ctypes.byref(a), _stream(q.device, stream))
+    _check("sparse_attn_decode_noalloc", st)
     return out
