@@ -85,24 +85,47 @@ int check_prefill(const sa_prefill_args* a)
 }
 
 // ---- decode workspace layout ----------------------------------------------
+// scores | zeroed block: key-bin histograms, candidate counters, split-K
+// tickets, scan tickets | threshold bins | kept-position bitmaps | candidate
+// lists | kept positions (if not returned) | split-K partials
 struct DecodeLayout {
     int splits;
-    size_t scores_off, idx_off, part_off, tickets_off, total;
+    int64_t ld_w, ld_s;
+    size_t scores_off, hist_off, cnt_off, tickets_off, row_tickets_off, zero_bytes, split_off, bitmap_off, cand_off,
+        idx_off, part_off, total;
 };
 
 DecodeLayout decode_layout(const sa_decode_args& a)
 {
     DecodeLayout l{};
     l.splits = sa::attention_splits(a.K, a.max_ctx, a.B);
+    const size_t B = (size_t)a.B;
+    const int64_t ctx = a.max_ctx > 0 ? a.max_ctx : 1;
+    l.ld_w = (ctx + 127) / 128 * 4;             // bitmap words per row, a multiple of 4
+    l.ld_s = l.ld_w * 32;                       // score row stride, a multiple of 128
     size_t off = 0;
     l.scores_off = off;
-    off += align_up(sizeof(float) * (size_t)a.B * (size_t)(a.max_ctx > 0 ? a.max_ctx : 1));
-    l.idx_off = off;
-    if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * (size_t)a.B * a.K);
-    l.part_off = off;
-    if (l.splits > 1) off += align_up(sizeof(float) * (size_t)a.B * l.splits * a.Hq * (a.dv + 2));
+    off += align_up(sizeof(float) * B * (size_t)l.ld_s);
+    l.hist_off = off;
+    off += sizeof(unsigned) * B * 4096;
+    l.cnt_off = off;
+    off += sizeof(unsigned) * B;
     l.tickets_off = off;
-    off += align_up(sizeof(unsigned) * (size_t)a.B * a.Hq);
+    off += sizeof(unsigned) * B * (size_t)a.Hq;
+    l.row_tickets_off = off;
+    off += sizeof(unsigned) * B;
+    off = align_up(off);
+    l.zero_bytes = off - l.hist_off;
+    l.split_off = off;
+    off += align_up(sizeof(sa::BinSplit) * B);
+    l.bitmap_off = off;
+    off += align_up(sizeof(uint32_t) * B * (size_t)l.ld_w);
+    l.cand_off = off;
+    off += align_up(sizeof(unsigned long long) * B * sa::DECODE_CAND_CAP);
+    l.idx_off = off;
+    if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * B * a.K);
+    l.part_off = off;
+    if (l.splits > 1) off += align_up(sizeof(float) * B * l.splits * a.Hq * (a.dv + 2));
     l.total = off;
     return l;
 }
@@ -253,23 +276,29 @@ int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes, cu
     if (!ws || ws_bytes < lay.total || !aligned(ws, WS_ALIGN)) return SA_ERR_WORKSPACE;
     char* wsb = static_cast<char*>(ws);
     float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
+    unsigned* hist = reinterpret_cast<unsigned*>(wsb + lay.hist_off);
+    unsigned* cand_cnt = reinterpret_cast<unsigned*>(wsb + lay.cnt_off);
+    unsigned* tickets = reinterpret_cast<unsigned*>(wsb + lay.tickets_off);
     int32_t* idx = a.idx_out ? a.idx_out : reinterpret_cast<int32_t*>(wsb + lay.idx_off);
     float* part = reinterpret_cast<float*>(wsb + lay.part_off);
-    unsigned* tickets = reinterpret_cast<unsigned*>(wsb + lay.tickets_off);
 
-    if (cudaMemsetAsync(tickets, 0, sizeof(unsigned) * (size_t)a.B * a.Hq, stream) != cudaSuccess)
-        return SA_ERR_LAUNCH;
+    if (sa::launch_zero(wsb + lay.hist_off, lay.zero_bytes, stream) != cudaSuccess) return SA_ERR_LAUNCH;
     sa::DecodeScanArgs da{};
     da.q_idx = a.q_idx; da.w = a.w; da.k_idx = a.k_idx_cache; da.seq_start = a.seq_start;
     da.ctx_len = a.ctx_len; da.max_ctx = a.max_ctx; da.B = a.B; da.Hi = a.Hi; da.di = a.di;
-    da.scores = scores; da.tickets = tickets;
+    da.scores = scores; da.ld_s = lay.ld_s; da.hist = hist;
+    da.row_tickets = reinterpret_cast<unsigned*>(wsb + lay.row_tickets_off); da.K = a.K;
+    da.split = reinterpret_cast<sa::BinSplit*>(wsb + lay.split_off);
     if (sa::launch_decode_scan(da, stream) != cudaSuccess) return SA_ERR_LAUNCH;
     if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
 
-    sa::TopkArgs ta{};
-    ta.scores = scores; ta.ld_s = a.max_ctx > 0 ? a.max_ctx : 1; ta.row_len = a.ctx_len;
-    ta.causal_first = 0; ta.n_cap = a.max_ctx; ta.rows = a.B; ta.K = a.K; ta.idx = idx; ta.ld_idx = a.K;
-    if (sa::launch_topk(ta, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    sa::DecodeSelectArgs sa_{};
+    sa_.scores = scores; sa_.ld_s = lay.ld_s; sa_.ctx_len = a.ctx_len;
+    sa_.max_ctx = a.max_ctx; sa_.B = a.B; sa_.K = a.K; sa_.split = da.split;
+    sa_.bitmap = reinterpret_cast<uint32_t*>(wsb + lay.bitmap_off); sa_.ld_w = lay.ld_w;
+    sa_.cand = reinterpret_cast<unsigned long long*>(wsb + lay.cand_off); sa_.cand_cap = sa::DECODE_CAND_CAP;
+    sa_.cand_cnt = cand_cnt; sa_.idx = idx;
+    if (sa::launch_decode_select(sa_, stream) != cudaSuccess) return SA_ERR_LAUNCH;
     if (a.stage_events && cudaEventRecord(a.stage_events[1], stream) != cudaSuccess) return SA_ERR_LAUNCH;
 
     sa::AttnArgs at{};
@@ -279,7 +308,7 @@ int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes, cu
     at.causal_first = 0; at.n_cap = a.max_ctx; at.gate = a.gate;
     at.rows = a.B; at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
     at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype; at.out = a.out;
-    at.splits = lay.splits; at.part = part; at.tickets = tickets;
+    at.splits = lay.splits; at.part = part; at.tickets = tickets; at.pdl = true;
     if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
     if (a.stage_events && cudaEventRecord(a.stage_events[2], stream) != cudaSuccess) return SA_ERR_LAUNCH;
     return SA_OK;

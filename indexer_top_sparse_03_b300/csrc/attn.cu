@@ -15,8 +15,7 @@
 // CTAs and the last CTA of a row, found through an atomic ticket, merges the
 // partial (max, sum, acc) triples with a log-sum-exp combine. Nothing waits
 // on another CTA.
-#include "common.cuh"
-#include "kernels.h"
+#include "attn_common.cuh"
 #include "../../include/sparse_attn.h"
 
 namespace sa {
@@ -25,68 +24,6 @@ namespace {
 constexpr int AT_THREADS = 128;     // 4 warps
 constexpr int CHUNK = 64;           // kept rows per pipeline stage
 constexpr int PAD = 8;              // bf16 elements of row padding (16 B)
-constexpr float LOG2E = 1.4426950408889634f;
-
-SA_DEVINL int64_t attn_hist_len(const AttnArgs& a, int r)
-{
-    int64_t n = a.ctx_len ? (int64_t)a.ctx_len[r] : a.causal_first + r + 1;
-    return n < 0 ? 0 : (n > a.n_cap ? a.n_cap : n);
-}
-
-SA_DEVINL int64_t attn_base(const AttnArgs& a, int r) { return a.row_base ? a.row_base[r] : 0; }
-
-SA_DEVINL float gate_of(const AttnArgs& a, int r, int h)
-{
-    const float x = a.gate[(int64_t)r * a.Hq + h];
-    return 1.0f / (1.0f + expf(-x));
-}
-
-template <typename T> SA_DEVINL void store_out(T* p, float v);
-template <> SA_DEVINL void store_out<float>(float* p, float v) { *p = v; }
-template <> SA_DEVINL void store_out<bf16>(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
-
-// Merge the split partials of heads [h0, h1) of row r (whole CTA).
-template <typename T>
-__device__ void combine_splits(const AttnArgs& a, int r, int h0, int h1)
-{
-    const int dv = a.dv, S = a.splits;
-    for (int e = threadIdx.x; e < (h1 - h0) * dv; e += blockDim.x) {
-        const int h = h0 + e / dv, col = e % dv;
-        float m = -INFINITY;
-        for (int s = 0; s < S; ++s) {
-            const float* p = a.part + (((int64_t)r * S + s) * a.Hq + h) * (dv + 2);
-            m = fmaxf(m, __ldcg(p + dv));
-        }
-        float L = 0.0f, O = 0.0f;
-        if (m != -INFINITY) {
-            for (int s = 0; s < S; ++s) {
-                const float* p = a.part + (((int64_t)r * S + s) * a.Hq + h) * (dv + 2);
-                const float ms = __ldcg(p + dv);
-                if (ms == -INFINITY) continue;
-                const float f = exp2f(ms - m);
-                L = fmaf(__ldcg(p + dv + 1), f, L);
-                O = fmaf(__ldcg(p + col), f, O);
-            }
-        }
-        const float o = L > 0.0f ? O / L : 0.0f;
-        store_out<T>(static_cast<T*>(a.out) + ((int64_t)r * a.Hq + h) * dv + col, gate_of(a, r, h) * o);
-    }
-}
-
-// Ticket: returns true in every thread of the CTA that finished row r's group last.
-SA_DEVINL bool take_ticket(unsigned* ticket, int splits, int* sh_flag)
-{
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned prev = atomicAdd(ticket, 1u);
-        *sh_flag = (prev == (unsigned)splits - 1u);
-    }
-    __syncthreads();
-    const bool last = *sh_flag != 0;
-    if (last) __threadfence();
-    return last;
-}
 
 // ---------------------------------------------------------------------------
 // bf16 tensor-core path (mma.sync m16n8k16); dv = 32 * NT, NT even
@@ -99,6 +36,8 @@ attn_mma_kernel(AttnArgs a)
     __shared__ float red_max[4][16], red_sum[4][16];
     __shared__ int sh_flag;
 
+    griddep_wait();                          // the kept positions
+    griddep_launch();
     const int r = blockIdx.x, split = blockIdx.y, hg = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
@@ -168,12 +107,17 @@ attn_mma_kernel(AttnArgs a)
     const int mat = lane >> 3, rr = lane & 7;
     const int colbase = warp * (dv / 4);
 
-    if (nchunks > 0) issue(0, 0);
+    // cp.async pipeline: chunk c lives in buffer c % stages; up to stages - 1
+    // chunks are in flight while one is being consumed
+    for (int c = 0; c < min(nchunks, max(stages - 1, 1)); ++c) issue(c, c);
     for (int c = 0; c < nchunks; ++c) {
-        const int buf = stages == 2 ? (c & 1) : 0;
-        cp_async_wait<0>();
+        const int buf = c % stages;
+        const int pending = min(nchunks - 1, c + stages - 2) - c;     // groups allowed in flight
+        if (pending >= 2) cp_async_wait<2>();
+        else if (pending == 1) cp_async_wait<1>();
+        else cp_async_wait<0>();
         __syncthreads();
-        if (stages == 2 && c + 1 < nchunks) issue(c + 1, buf ^ 1);
+        if (stages >= 2 && c + stages - 1 < nchunks) issue(c + stages - 1, (c + stages - 1) % stages);
 
         const bf16* Kb = Ks + buf * CHUNK * ks_ld;
         const bf16* Vb = a.v_aliases_k ? Kb : Vs + buf * CHUNK * vs_ld;
@@ -308,6 +252,8 @@ attn_simt_kernel(AttnArgs a)
     __shared__ int64_t prow[AT_THREADS];
     __shared__ float red[AT_THREADS / 32];
     __shared__ int sh_flag;
+    griddep_wait();
+    griddep_launch();
     const int r = blockIdx.x, split = blockIdx.y, h = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int dqk = a.dqk, dv = a.dv;
@@ -406,10 +352,17 @@ size_t mma_smem_bytes(const AttnArgs& a, int stages)
 
 constexpr size_t MMA_SMEM_LIMIT = 200 * 1024;    // leaves room for static shared memory
 
+// Pipeline depth: double buffering (the kernel supports up to 4 buffers).
+int attention_stages(const AttnArgs& a)
+{
+    // measured: more CTAs per SM beat a deeper pipeline in one CTA
+    return mma_smem_bytes(a, 2) <= MMA_SMEM_LIMIT ? 2 : 1;
+}
+
 template <int NT>
 cudaError_t launch_mma(AttnArgs a, cudaStream_t s)
 {
-    a.stages = mma_smem_bytes(a, 2) <= MMA_SMEM_LIMIT ? 2 : 1;
+    a.stages = attention_stages(a);
     const size_t smem = mma_smem_bytes(a, a.stages);
     cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) {
@@ -417,8 +370,7 @@ cudaError_t launch_mma(AttnArgs a, cudaStream_t s)
         return e;
     }
     dim3 grid(a.rows, a.splits, (a.Hq + 15) / 16);
-    attn_mma_kernel<NT><<<grid, AT_THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(attn_mma_kernel<NT>, grid, dim3(AT_THREADS), smem, s, a.pdl, a);
 }
 
 }  // namespace
@@ -442,13 +394,18 @@ int attention_splits(int K, int64_t n_cap, int rows)
     if (kept <= 256 || rows <= 0 || rows >= target) return 1;
     const int want = (target + rows - 1) / rows;
     int64_t per = (kept + want - 1) / want;
-    per = max64(256, (per + CHUNK - 1) / CHUNK * CHUNK);
+    per = max64(max64(256, (K + MAX_SPLITS - 1) / MAX_SPLITS), per);
+    per = (per + CHUNK - 1) / CHUNK * CHUNK;
     return (int)((K + per - 1) / per);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s)
 {
     if (a.rows <= 0) return cudaSuccess;
+    if (attention_gather_supported(a)) {
+        const cudaError_t e = launch_attention_gather(a, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (attention_mma_supported(a)) {
         switch (a.dv / 32) {
         case 2: return launch_mma<2>(a, s);
@@ -462,9 +419,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s)
     }
     dim3 grid(a.rows, a.splits, a.Hq);
     const size_t smem = sizeof(float) * a.dqk;
-    if (a.dtype == SA_F32) attn_simt_kernel<float><<<grid, AT_THREADS, smem, s>>>(a);
-    else attn_simt_kernel<bf16><<<grid, AT_THREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    if (a.dtype == SA_F32) return launch_kernel(attn_simt_kernel<float>, grid, dim3(AT_THREADS), smem, s, a.pdl, a);
+    return launch_kernel(attn_simt_kernel<bf16>, grid, dim3(AT_THREADS), smem, s, a.pdl, a);
 }
 
 }  // namespace sa

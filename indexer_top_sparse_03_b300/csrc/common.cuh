@@ -96,6 +96,31 @@ SA_DEVINL uint4 ldg_stream16(const void* p)
     return v;
 }
 
+// L2 policy for data read exactly once (streamed caches): evicted first, so
+// that data reused soon (score rows, gathered K/V) stays resident.
+SA_DEVINL uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+SA_DEVINL uint4 ldg_stream16_hint(const void* p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+    return v;
+}
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor finishes;
+// griddep_wait() blocks until the predecessor grid has completed and its
+// memory is visible (a no-op without the attribute), griddep_launch() lets
+// the successor start launching.
+SA_DEVINL void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SA_DEVINL void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 SA_DEVINL float warp_max(float v)
 {
 #pragma unroll

@@ -15,15 +15,22 @@
 // no shared-memory staging, and q's B fragments use the same mapping.
 //   k-step kk, fragment column c  ->  dim 32*(kk/2) + 8*((c%8)/2)
 //                                        + 4*(kk%2) + 2*(c/8) + c%2
+//
+// Every CTA also counts its scores into a 4096-bin histogram of the top 12
+// bits of their order-preserving keys (shared-memory atomics), and adds the
+// non-zero bins to the sequence's histogram in global memory: the Top-K
+// step reads that histogram to find the bin of the K-th best score without
+// another pass over the scores.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk_core.cuh"
 
 namespace sa {
 namespace {
 
 constexpr int SCAN_THREADS = 256;           // 8 warps
 constexpr int SCAN_CHUNK = 4096;            // keys per CTA
-constexpr int SCAN_UNROLL = 4;              // 16-key groups in flight per warp
+constexpr int scan_unroll(int di) { return di <= 64 ? 4 : (di == 128 ? 2 : 1); }   // 16-key groups in flight per warp
 
 template <int DI, int NTH>
 __global__ void __launch_bounds__(SCAN_THREADS)
@@ -31,6 +38,9 @@ decode_scan_kernel(DecodeScanArgs a)
 {
     constexpr int KS = DI / 16;              // k-steps
     constexpr int VM = DI / 32;              // 16-byte pieces per key row per lane
+    constexpr int SCAN_UNROLL_DI = scan_unroll(DI);
+    griddep_wait();                          // the zeroed histogram and tickets
+    griddep_launch();
     const int b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
@@ -39,6 +49,9 @@ decode_scan_kernel(DecodeScanArgs a)
     const int64_t j0 = (int64_t)blockIdx.x * SCAN_CHUNK;
     if (j0 >= n) return;
     const int cnt = (int)min64(SCAN_CHUNK, n - j0);
+    __shared__ unsigned sh_hist[HBINS];
+    for (int i = tid; i < HBINS; i += SCAN_THREADS) sh_hist[i] = 0;
+    __syncthreads();
 
     // q fragments (B operand) and head weights held by this lane
     const bf16* q = static_cast<const bf16*>(a.q_idx) + (int64_t)b * a.Hi * DI;
@@ -66,22 +79,23 @@ decode_scan_kernel(DecodeScanArgs a)
     }
 
     const bf16* kb = static_cast<const bf16*>(a.k_idx) + (a.seq_start[b] + j0) * DI;
-    float* sc = a.scores + (int64_t)b * a.max_ctx + j0;
-    constexpr int STEP = 8 * 16 * SCAN_UNROLL;   // keys per CTA iteration
+    float* sc = a.scores + (int64_t)b * a.ld_s + j0;
+    constexpr int STEP = 8 * 16 * SCAN_UNROLL_DI;   // keys per CTA iteration
 
+    const uint64_t pol = l2_evict_first_policy();
     for (int base = warp * 16; base < cnt; base += STEP) {
-        uint4 va[SCAN_UNROLL][VM], vb[SCAN_UNROLL][VM];
+        uint4 va[SCAN_UNROLL_DI][VM], vb[SCAN_UNROLL_DI][VM];
 #pragma unroll
-        for (int u = 0; u < SCAN_UNROLL; ++u) {
+        for (int u = 0; u < SCAN_UNROLL_DI; ++u) {
             const int k0 = base + u * 8 * 16 + g, k1 = k0 + 8;
 #pragma unroll
             for (int m = 0; m < VM; ++m) {
-                va[u][m] = k0 < cnt ? ldg_stream16(kb + (int64_t)k0 * DI + 32 * m + 8 * t4) : make_uint4(0, 0, 0, 0);
-                vb[u][m] = k1 < cnt ? ldg_stream16(kb + (int64_t)k1 * DI + 32 * m + 8 * t4) : make_uint4(0, 0, 0, 0);
+                va[u][m] = k0 < cnt ? ldg_stream16_hint(kb + (int64_t)k0 * DI + 32 * m + 8 * t4, pol) : make_uint4(0, 0, 0, 0);
+                vb[u][m] = k1 < cnt ? ldg_stream16_hint(kb + (int64_t)k1 * DI + 32 * m + 8 * t4, pol) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
-        for (int u = 0; u < SCAN_UNROLL; ++u) {
+        for (int u = 0; u < SCAN_UNROLL_DI; ++u) {
             float acc[NTH][4];
 #pragma unroll
             for (int nt = 0; nt < NTH; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
@@ -110,24 +124,64 @@ decode_scan_kernel(DecodeScanArgs a)
             s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
             const int k0 = base + u * 8 * 16 + g, k1 = k0 + 8;
             if (t4 == 0) {
-                if (k0 < cnt) sc[k0] = s0;
-                if (k1 < cnt) sc[k1] = s1;
+                if (k0 < cnt) { sc[k0] = s0; atomicAdd(&sh_hist[key_bin(score_key(s0))], 1u); }
+                if (k1 < cnt) { sc[k1] = s1; atomicAdd(&sh_hist[key_bin(score_key(s1))], 1u); }
             }
         }
     }
+    __syncthreads();
+    unsigned* gh = a.hist + (int64_t)b * HBINS;
+    for (int i = tid; i < HBINS; i += SCAN_THREADS) {
+        const unsigned c = sh_hist[i];
+        if (c) atomicAdd(gh + i, c);
+    }
+
+    // the last CTA of the row (atomic ticket; nothing waits) finds the bin of
+    // the K-th best score once, for the Top-K step
+    __shared__ int sh_last;
+    __shared__ unsigned warp_tot[32];
+    __shared__ BinSplit split;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned ctas = (unsigned)((n + SCAN_CHUNK - 1) / SCAN_CHUNK);
+        sh_last = atomicAdd(a.row_tickets + b, 1u) == ctas - 1u;
+    }
+    __syncthreads();
+    if (!sh_last) return;
+    __threadfence();
+    stage_hist(sh_hist, gh);
+    const BinSplit bs = find_bin(sh_hist, (unsigned)a.K, warp_tot, &split);
+    if (tid == 0) a.split[b] = bs;
+}
+
+__global__ void __launch_bounds__(256)
+zero_kernel(uint4* p, size_t n16)
+{
+    griddep_launch();
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+        p[i] = make_uint4(0, 0, 0, 0);
 }
 
 template <int DI>
 cudaError_t launch_di(const DecodeScanArgs& a, cudaStream_t s)
 {
     dim3 grid((unsigned)((a.max_ctx + SCAN_CHUNK - 1) / SCAN_CHUNK), a.B);
-    if (a.Hi <= 8) decode_scan_kernel<DI, 1><<<grid, SCAN_THREADS, 0, s>>>(a);
-    else if (a.Hi <= 16) decode_scan_kernel<DI, 2><<<grid, SCAN_THREADS, 0, s>>>(a);
-    else decode_scan_kernel<DI, 4><<<grid, SCAN_THREADS, 0, s>>>(a);
-    return cudaGetLastError();
+    if (a.Hi <= 8) return launch_kernel(decode_scan_kernel<DI, 1>, grid, dim3(SCAN_THREADS), 0, s, true, a);
+    if (a.Hi <= 16) return launch_kernel(decode_scan_kernel<DI, 2>, grid, dim3(SCAN_THREADS), 0, s, true, a);
+    return launch_kernel(decode_scan_kernel<DI, 4>, grid, dim3(SCAN_THREADS), 0, s, true, a);
 }
 
 }  // namespace
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s)
+{
+    const size_t n16 = bytes / 16;
+    if (n16 == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)min64(1184, (int64_t)((n16 + 255) / 256));
+    zero_kernel<<<blocks, 256, 0, s>>>(static_cast<uint4*>(p), n16);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode_scan(const DecodeScanArgs& a, cudaStream_t s)
 {

@@ -132,6 +132,7 @@ cudaError_t launch_indexer_simt(const IndexerArgs& a, cudaStream_t s)
 
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s)
 {
+    if (indexer_tc_supported(a)) return launch_indexer_tc(a, s);
     return launch_indexer_simt(a, s);
 }
 

@@ -1,0 +1,468 @@
+// Indexer score on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   s[t, j] = sum_h w[t,h] * max(0, q_idx[t,h,:] . k_idx[j,:])     (j < n_t)
+//
+// The light relevance score of every query against every causal history
+// position ("Hybrid Attention Architectures...", section 3.1, indexing stage;
+// no positional encoding, "From Full Attention to Sparsity", indexer
+// paragraph). For FP8 inputs each stored row carries a positive fp32 scale;
+// the query scale is folded into the head weight and the key scale multiplies
+// the finished head sum (a positive factor commutes with the ReLU).
+//
+// Tile = 128 keys (the MMA's M side, one TMEM lane per key) x 256 (query,
+// head) pairs (the N side: q_idx viewed as a [T*Hi, di] matrix already lists
+// the pairs of consecutive queries). With this orientation the head sum of a
+// (key, query) score lies in the registers of the one thread that owns the
+// key's TMEM lane, so the epilogue needs no cross-thread reduction, and its
+// stores are coalesced (a warp writes 32 consecutive keys of one query).
+//
+// Persistent CTAs, one per SM, each walking a static stride of work items
+// (query tile, group of up to 8 key tiles; key tiles wholly outside the
+// causal window are never visited). Warp roles:
+//   warp 0      TMA producer: query tile once per item, key tiles through a
+//               ring of shared-memory stages (128-byte-swizzled K-major tiles)
+//   warp 1      TMEM owner (512 columns = two 128x256 fp32 accumulators) and
+//               MMA issuer (one thread, kind::f16 or kind::f8f6f4)
+//   warps 2-9   epilogue: TMEM -> registers, ReLU, weighted head sum, causal
+//               mask, fp32 store; two warps per TMEM sub-partition, each
+//               taking half of the 256 columns
+// Accumulators are double-buffered so that the epilogue of one key tile
+// overlaps the MMAs of the next. Every wait is bounded (see tc.cuh).
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+#include "../../include/sparse_attn.h"
+
+namespace sa {
+
+// error word of the bounded waits (read back by sa_device_errors)
+__device__ unsigned g_tc_error = 0;
+
+namespace {
+
+constexpr int TC_BM = 128;                 // keys per tile (MMA M)
+constexpr int TC_BN = 256;                 // (query, head) pairs per tile (MMA N)
+constexpr int TC_GROUP = 8;                // key tiles per work item
+constexpr int TC_EPI_WARPS = 8;
+constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
+
+template <int ES, int DI, int HI>
+struct TcCfg {
+    static constexpr int TQ = TC_BN / HI;                  // queries per tile
+    static constexpr int ROWB = DI * ES;                   // bytes per operand row
+    static constexpr int KB = ROWB < 128 ? ROWB : 128;     // K-block bytes = swizzle span
+    static constexpr int NKB = ROWB / KB;
+    static constexpr int KSTEPS = KB / 32;                 // MMAs per K-block (K = 32 bytes)
+    static constexpr int A_BYTES = TC_BM * ROWB;
+    static constexpr int B_BYTES = TC_BN * ROWB;
+    static constexpr int STAGES = (A_BYTES <= 16384) ? 4 : 3;
+    static constexpr int B_BUFS = (STAGES * A_BYTES + 2 * B_BYTES <= 160 * 1024) ? 2 : 1;
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_W = OFF_B + B_BUFS * B_BYTES;
+    static constexpr int OFF_BAR = OFF_W + TC_BN * 4;
+    // + barriers and alignment slack; never less than 116 KB, so that two CTAs
+    // cannot share an SM (each holds all 512 TMEM columns)
+    static constexpr int SMEM_NEED = OFF_BAR + 256 + 1024;
+    static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
+    static constexpr uint32_t IDESC = mma_idesc(ES == 2 ? 1u : 0u, TC_BM, TC_BN);
+    static_assert(ROWB % KB == 0 && KB >= 32, "operand rows must be 32, 64 or a multiple of 128 bytes");
+};
+
+// Work items: query tile qi (TQ queries from t_begin + qi*TQ) x group g of
+// TC_GROUP key tiles. The walk below visits item blockIdx.x, then every
+// gridDim.x-th item after it, in (qi, g) order.
+struct ItemWalk {
+    int qi, g;
+};
+
+template <int TQ>
+SA_DEVINL int item_groups(const IndexerArgs& a, int qi)
+{
+    const int64_t t0 = (int64_t)a.t_begin + (int64_t)qi * TQ;
+    const int64_t t_last = min64(t0 + TQ, a.T) - 1;
+    const int64_t n_last = min64(a.N, max64(0, t_last + 1 + a.causal_offset));
+    const int64_t tiles = (n_last + TC_BM - 1) / TC_BM;
+    return (int)((tiles + TC_GROUP - 1) / TC_GROUP);
+}
+
+template <int TQ>
+SA_DEVINL bool item_advance(const IndexerArgs& a, int nq, ItemWalk& w, int step)
+{
+    w.g += step;
+    while (w.qi < nq) {
+        const int ng = item_groups<TQ>(a, w.qi);
+        if (w.g < ng) return true;
+        w.g -= ng;
+        ++w.qi;
+    }
+    return false;
+}
+
+// Weighted ReLU head sum of one (key, query) score from its HI accumulator
+// columns; w holds the query's HI head weights (16-byte aligned). With four or
+// more heads the sum runs on packed fp32x2 lanes (two heads per instruction).
+template <int HI>
+SA_DEVINL float head_sum(const uint32_t* r, const float* w)
+{
+    if constexpr (HI >= 4) {
+        unsigned long long acc2 = 0ull;
+#pragma unroll
+        for (int h4 = 0; h4 < HI; h4 += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(w + h4);
+            acc2 = f32x2_fma(f32x2_pack(fmaxf(__uint_as_float(r[h4]), 0.0f), fmaxf(__uint_as_float(r[h4 + 1]), 0.0f)),
+                             f32x2_pack(w4.x, w4.y), acc2);
+            acc2 = f32x2_fma(f32x2_pack(fmaxf(__uint_as_float(r[h4 + 2]), 0.0f), fmaxf(__uint_as_float(r[h4 + 3]), 0.0f)),
+                             f32x2_pack(w4.z, w4.w), acc2);
+        }
+        const float2 s2 = f32x2_unpack(acc2);
+        return s2.x + s2.y;
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < HI; ++h) s = fmaf(w[h], fmaxf(__uint_as_float(r[h]), 0.0f), s);
+        return s;
+    }
+}
+
+// Epilogue of one accumulator tile for one thread: its key's 128 columns
+// (128 / HI queries), read from TMEM 64 columns at a time; the accumulator is
+// released as soon as the last columns are in registers. FULL tiles lie inside
+// every query's causal window; the others test each (query, key) pair:
+// store iff t < T, j < N and j <= t + off.
+template <int HI, bool FULL, bool FP8>
+SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int64_t ld_s, int64_t j,
+                        int t_first, int T, int64_t off, uint64_t* empty_bar, int64_t N = 0)
+{
+    constexpr int QPH = 64 / HI;                       // queries per 64 columns
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + hc * 64, ra);
+        tmem_ld32(taddr + hc * 64 + 32, rb);
+        tmem_ld_wait();
+        if (hc == 1) {
+            tc_fence_before();
+            mbar_arrive(empty_bar);
+        }
+#pragma unroll
+        for (int qq = 0; qq < QPH; ++qq) {
+            const uint32_t* r = qq < QPH / 2 ? &ra[qq * HI] : &rb[(qq - QPH / 2) * HI];
+            float s = head_sum<HI>(r, w + (hc * QPH + qq) * HI);
+            if (FP8) s *= ks;
+            if (FULL) {
+                *p = s;
+            } else {
+                const int t = t_first + hc * QPH + qq;
+                if (t < T && j < N && j <= (int64_t)t + off) *p = s;
+            }
+            p += ld_s;
+        }
+    }
+}
+
+template <int ES, int DI, int HI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                  IndexerArgs a)
+{
+    using C = TcCfg<ES, DI, HI>;
+    constexpr int TQ = C::TQ;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::OFF_B;
+    float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* a_full = bars;                       // [STAGES]
+    uint64_t* a_empty = bars + C::STAGES;          // [STAGES]
+    uint64_t* b_full = bars + 2 * C::STAGES;       // [2]
+    uint64_t* b_empty = b_full + 2;                // [2]
+    uint64_t* acc_full = b_empty + 2;              // [2]
+    uint64_t* acc_empty = acc_full + 2;            // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nq = (a.T - a.t_begin + TQ - 1) / TQ;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1);
+            mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS * 32);
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    ItemWalk it{0, 0};
+    bool have = item_advance<TQ>(a, nq, it, blockIdx.x);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0, bb = 0;
+            uint32_t aph = 0, bph = 0;
+            for (; have; have = item_advance<TQ>(a, nq, it, gridDim.x)) {
+                const int t0 = a.t_begin + it.qi * TQ;
+                const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
+                const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
+                if (!mbar_wait(&b_empty[bb], bph ^ 1, &g_tc_error)) break;
+                mbar_arrive_expect_tx(&b_full[bb], C::B_BYTES);
+                uint8_t* bdst = sB + (C::B_BUFS == 2 ? bb : 0) * C::B_BYTES;
+                for (int kb = 0; kb < C::NKB; ++kb)
+                    tma_load_2d(bdst + kb * TC_BN * C::KB, &tm_q, kb * (C::KB / ES), t0 * HI, &b_full[bb]);
+                bool ok = true;
+                for (int kt = k_begin; kt < k_end; ++kt) {
+                    if (!mbar_wait(&a_empty[s], aph ^ 1, &g_tc_error)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&a_full[s], C::A_BYTES);
+                    uint8_t* adst = sA + s * C::A_BYTES;
+                    for (int kb = 0; kb < C::NKB; ++kb)
+                        tma_load_2d(adst + kb * TC_BM * C::KB, &tm_k, kb * (C::KB / ES), kt * TC_BM, &a_full[s]);
+                    if (++s == C::STAGES) { s = 0; aph ^= 1; }
+                }
+                if (!ok) break;
+                if (C::B_BUFS == 2) { bb ^= 1; if (bb == 0) bph ^= 1; } else { bph ^= 1; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0, bb = 0, ab = 0;
+            uint32_t aph = 0, bph = 0, acph = 0;
+            for (; have; have = item_advance<TQ>(a, nq, it, gridDim.x)) {
+                const int t0 = a.t_begin + it.qi * TQ;
+                const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
+                const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
+                if (!mbar_wait(&b_full[bb], bph, &g_tc_error)) break;
+                tc_fence_after();
+                const uint32_t b_base = smem_u32(sB + (C::B_BUFS == 2 ? bb : 0) * C::B_BYTES);
+                bool ok = true;
+                for (int kt = k_begin; kt < k_end; ++kt) {
+                    if (!mbar_wait(&a_full[s], aph, &g_tc_error) || !mbar_wait(&acc_empty[ab], acph ^ 1, &g_tc_error)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
+                    const uint32_t d = tmem + (uint32_t)(ab * TC_BN);
+#pragma unroll
+                    for (int kb = 0; kb < C::NKB; ++kb) {
+#pragma unroll
+                        for (int ks = 0; ks < C::KSTEPS; ++ks) {
+                            const uint64_t ad = smem_desc_kmajor(a_base + kb * TC_BM * C::KB + ks * 32, C::KB);
+                            const uint64_t bd = smem_desc_kmajor(b_base + kb * TC_BN * C::KB + ks * 32, C::KB);
+                            const uint32_t acc = (kb | ks) != 0;
+                            if (ES == 2) tc_mma_f16(d, ad, bd, C::IDESC, acc);
+                            else tc_mma_f8(d, ad, bd, C::IDESC, acc);
+                        }
+                    }
+                    tc_commit(&a_empty[s]);          // smem stage free once these MMAs finish
+                    tc_commit(&acc_full[ab]);        // accumulator ready for the epilogue
+                    if (++s == C::STAGES) { s = 0; aph ^= 1; }
+                    ab ^= 1;
+                    if (ab == 0) acph ^= 1;
+                }
+                if (!ok) break;
+                tc_commit(&b_empty[bb]);
+                if (C::B_BUFS == 2) { bb ^= 1; if (bb == 0) bph ^= 1; } else { bph ^= 1; }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = threadIdx.x - 64;                 // 0 .. 255
+        const int sub = warp & 3;                       // TMEM sub-partition of this warp
+        const int half = (warp - 2) >> 2;               // which 128 columns
+        const int row = sub * 32 + lane;                // TMEM lane = key within the tile
+        const bool fp8 = (ES == 1);
+        int ab = 0;
+        uint32_t acph = 0;
+        bool ok = true;
+        // After a timed-out wait the loop keeps its shape (same named-barrier
+        // count in every epilogue warp) but touches neither TMEM nor memory.
+        for (; have; have = item_advance<TQ>(a, nq, it, gridDim.x)) {
+            const int t0 = a.t_begin + it.qi * TQ;
+            const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
+            const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
+            // head weights of this query tile (FP8: times the query-row scale)
+            asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
+            for (int i = e; i < TC_BN; i += TC_EPI_WARPS * 32) {
+                const int t = t0 + i / HI;
+                float wv = 0.0f;
+                if (t < a.T) {
+                    wv = a.w[(int64_t)t * HI + (i % HI)];
+                    if (fp8) wv *= a.q_scale[(int64_t)t * HI + (i % HI)];
+                }
+                sW[i] = wv;
+            }
+            asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
+
+            // tiles whose every key is visible to every query of the tile
+            // skip the per-query causal mask
+            const int64_t n_first = min64(a.N, max64(0, (int64_t)t0 + 1 + a.causal_offset));
+            const bool rows_full = t0 + TQ <= a.T;
+            const int tq_first = half * (128 / HI);
+            for (int kt = k_begin; kt < k_end; ++kt) {
+                const int64_t j = (int64_t)kt * TC_BM + row;
+                const float ks = (fp8 && j < a.N) ? a.k_scale[j] : 1.0f;
+                const bool full = rows_full && (int64_t)kt * TC_BM + TC_BM <= n_first;
+                if (ok) ok = mbar_wait(&acc_full[ab], acph, &g_tc_error);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) continue;
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * 128);
+                float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
+                const float* w_half = sW + tq_first * HI;
+                if (full)
+                    epi_tile<HI, true, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, 0, 0, 0, &acc_empty[ab]);
+                else
+                    epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a.T,
+                                                 a.causal_offset, &acc_empty[ab], a.N);
+                ab ^= 1;
+                if (ab == 0) acph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int ES, int DI, int HI>
+cudaError_t launch_tc(const IndexerArgs& a, cudaStream_t s)
+{
+    using C = TcCfg<ES, DI, HI>;
+    CUtensorMap tk, tq;
+    if (!make_tensor_map_2d(&tk, a.k_idx, ES, a.N, DI, DI, C::KB / ES, TC_BM) ||
+        !make_tensor_map_2d(&tq, a.q_idx, ES, (int64_t)a.T * HI, DI, DI, C::KB / ES, TC_BN))
+        return cudaErrorNotSupported;
+    // number of work items (host mirror of item_groups)
+    const int nq = (a.T - a.t_begin + C::TQ - 1) / C::TQ;
+    int64_t items = 0;
+    for (int qi = 0; qi < nq; ++qi) {
+        const int64_t t0 = (int64_t)a.t_begin + (int64_t)qi * C::TQ;
+        const int64_t t_last = min64(t0 + C::TQ, a.T) - 1;
+        const int64_t n_last = min64(a.N, max64(0, t_last + 1 + a.causal_offset));
+        items += ((n_last + TC_BM - 1) / TC_BM + TC_GROUP - 1) / TC_GROUP;
+    }
+    if (items == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<ES, DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return e;
+    }
+    const int grid = (int)min64(items, device_sm_count());
+    indexer_tc_kernel<ES, DI, HI><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, a);
+    return cudaGetLastError();
+}
+
+template <int ES, int DI>
+cudaError_t launch_tc_hi(const IndexerArgs& a, cudaStream_t s)
+{
+    switch (a.Hi) {
+    case 1: return launch_tc<ES, DI, 1>(a, s);
+    case 2: return launch_tc<ES, DI, 2>(a, s);
+    case 4: return launch_tc<ES, DI, 4>(a, s);
+    case 8: return launch_tc<ES, DI, 8>(a, s);
+    case 16: return launch_tc<ES, DI, 16>(a, s);
+    case 32: return launch_tc<ES, DI, 32>(a, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host helpers shared with the other TMA kernels
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, int64_t cols,
+                        int64_t row_stride_elems, int box_cols, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * elem_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const int span = box_cols * elem_bytes;
+    const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : span == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    return n;
+}
+
+bool indexer_tc_supported(const IndexerArgs& a)
+{
+    const bool hi_ok = a.Hi == 1 || a.Hi == 2 || a.Hi == 4 || a.Hi == 8 || a.Hi == 16 || a.Hi == 32;
+    if (!hi_ok) return false;
+    if (a.dtype == SA_BF16) return a.di == 16 || a.di == 32 || a.di == 64 || a.di == 128;
+    if (a.dtype == SA_FP8_E4M3) return a.di == 32 || a.di == 64 || a.di == 128 || a.di == 256;
+    return false;
+}
+
+cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t s)
+{
+    if (a.T - a.t_begin <= 0 || a.N <= 0) return cudaSuccess;
+    if (a.dtype == SA_BF16) {
+        switch (a.di) {
+        case 16: return launch_tc_hi<2, 16>(a, s);
+        case 32: return launch_tc_hi<2, 32>(a, s);
+        case 64: return launch_tc_hi<2, 64>(a, s);
+        case 128: return launch_tc_hi<2, 128>(a, s);
+        default: break;
+        }
+    } else if (a.dtype == SA_FP8_E4M3) {
+        switch (a.di) {
+        case 32: return launch_tc_hi<1, 32>(a, s);
+        case 64: return launch_tc_hi<1, 64>(a, s);
+        case 128: return launch_tc_hi<1, 128>(a, s);
+        case 256: return launch_tc_hi<1, 256>(a, s);
+        default: break;
+        }
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace sa

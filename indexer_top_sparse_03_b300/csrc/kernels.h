@@ -2,10 +2,42 @@
 // are validated by the C-ABI layer (api.cu) before any of these is called.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace sa {
+
+// 2D TMA descriptor of a row-major matrix of 1- or 2-byte elements (bf16 or
+// bytes); swizzle = the box's row bytes when 32, 64 or 128, else none.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, int64_t cols,
+                        int64_t row_stride_elems, int box_cols, int box_rows);
+int device_sm_count();
+
+// Kernel launch, optionally as a programmatic dependent of the previous work
+// on the stream (the kernel must call griddep_wait() before touching data
+// that work produces or reads).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
+// Zeroes `bytes` (a multiple of 16) at p; first kernel of the decode step.
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 
 // ---- step 1: indexer (prefill / shared keys) ------------------------------
 struct IndexerArgs {
@@ -21,7 +53,10 @@ struct IndexerArgs {
     float* scores;          // row t at scores + (t - t_begin) * ld_s
     int64_t ld_s;
 };
-cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
+cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);        // picks one of:
+cudaError_t launch_indexer_simt(const IndexerArgs& a, cudaStream_t s);   // any dtype/shape, CUDA cores
+cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t s);     // bf16 / FP8, tensor cores
+bool indexer_tc_supported(const IndexerArgs& a);
 
 // ---- step 2: Top-K over score rows -----------------------------------------
 struct TopkArgs {
@@ -60,9 +95,20 @@ struct AttnArgs {
     float* part;            // [rows, splits, Hq, dv + 2]
     unsigned* tickets;      // [rows], zero on entry, left zero on exit
     int stages;             // set by the launcher: gather buffers (1 or 2)
+    bool pdl;               // launch as a programmatic dependent of the previous kernel
 };
-cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);          // picks one of:
+bool attention_gather_supported(const AttnArgs& a);                       // TMA gather4, dv <= 128
+cudaError_t launch_attention_gather(const AttnArgs& a, cudaStream_t s);
 int attention_splits(int K, int64_t n_cap, int rows);
+
+// Bin of the K-th best score of a row, from a 4096-bin histogram of the top
+// 12 bits of the scores' order-preserving keys.
+struct BinSplit {
+    int bin;            // bin of the K-th best key
+    unsigned above;     // keys in higher bins (< K)
+    unsigned in_bin;    // keys in that bin (above + in_bin >= K)
+};
 
 // ---- decode step 1: indexer scan over each sequence's cache --------------
 struct DecodeScanArgs {
@@ -73,9 +119,31 @@ struct DecodeScanArgs {
     const int32_t* ctx_len;
     int64_t max_ctx;
     int B, Hi, di;
-    float* scores;          // [B, max_ctx]
-    unsigned* tickets;      // [B] zeroed here for the attention combine
+    float* scores;          // [B, ld_s]
+    int64_t ld_s;           // a multiple of 128 (rows 512-byte aligned)
+    unsigned* hist;         // [B, 4096] key-bin histogram, zero on entry
+    unsigned* row_tickets;  // [B], zero on entry
+    int K;
+    BinSplit* split;        // [B] bin of the K-th best score (rows with n > K)
 };
 cudaError_t launch_decode_scan(const DecodeScanArgs& a, cudaStream_t s);
+
+// ---- decode step 2: Top-K of each sequence's score row --------------------
+struct DecodeSelectArgs {
+    const float* scores;    // [B, ld_s], ld_s a multiple of 32
+    int64_t ld_s;
+    const int32_t* ctx_len;
+    int64_t max_ctx;
+    int B, K;
+    const BinSplit* split;  // [B] from the scan
+    uint32_t* bitmap;       // [B, ld_w] kept-position bits
+    int64_t ld_w;
+    unsigned long long* cand;   // [B, cand_cap] (key << 32 | ~position) of the threshold bin
+    int cand_cap;
+    unsigned* cand_cnt;     // [B], zero on entry
+    int32_t* idx;           // [B, K]
+};
+cudaError_t launch_decode_select(const DecodeSelectArgs& a, cudaStream_t s);
+constexpr int DECODE_CAND_CAP = 16384;
 
 }  // namespace sa

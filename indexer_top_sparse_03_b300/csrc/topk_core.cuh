@@ -1,0 +1,223 @@
+// Device pieces of the exact Top-K ("Hybrid Attention Architectures...",
+// section 3.1, filtering stage: keep the K highest-scoring positions; an
+// exact tie goes to the lower position).
+//
+// Scores are compared through order-preserving 32-bit keys (score_key). Two
+// selection schemes share these pieces:
+//   - a block-wide MSB-first radix select over one row (8-bit digits), used
+//     for short rows staged in shared memory and as the general fallback;
+//   - a threshold-bin scheme for long rows: a 4096-bin histogram of the key's
+//     top 12 bits gives the bin holding the K-th best score, every position in
+//     a higher bin is kept, and only the positions inside that bin are ranked
+//     exactly (by key, then by lower position).
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sa {
+
+constexpr int RADIX = 256;
+constexpr int HBITS = 12;                       // bits of the threshold-bin histogram
+constexpr int HBINS = 1 << HBITS;
+constexpr int HSHIFT = 32 - HBITS;
+
+SA_DEVINL uint32_t key_bin(uint32_t key) { return key >> HSHIFT; }
+
+// Inclusive prefix sum over the threads of the block (any multiple of 32 up
+// to 1024 threads); `warp_tot` is 32 words of shared scratch. Contains two
+// __syncthreads.
+SA_DEVINL unsigned block_scan_incl(unsigned v, unsigned* warp_tot, unsigned* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    unsigned before = 0, all = 0;
+    for (int w = 0; w < nw; ++w) {
+        const unsigned t = warp_tot[w];
+        before += (w < warp) ? t : 0u;
+        all += t;
+    }
+    __syncthreads();
+    if (total) *total = all;
+    return v + before;
+}
+
+// Copies a 4096-bin histogram from global memory into shared memory with
+// 16-byte loads (whole block; ends with __syncthreads).
+SA_DEVINL void stage_hist(unsigned* dst, const unsigned* src)
+{
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int i = threadIdx.x; i < HBINS / 4; i += blockDim.x) d4[i] = __ldcg(s4 + i);
+    __syncthreads();
+}
+
+// The bin holding the K-th largest key of a 4096-bin shared-memory histogram
+// with at least K entries (bins counted from the top). `out` is shared
+// scratch that receives the answer. Whole block.
+SA_DEVINL BinSplit find_bin(const unsigned* hist, unsigned K, unsigned* warp_tot, BinSplit* out)
+{
+    if (threadIdx.x == 0) { out->bin = 0; out->above = 0; out->in_bin = 0; }
+    const int per = HBINS / blockDim.x;            // bins per thread (4 .. 16)
+    const int top = HBINS - 1 - threadIdx.x * per; // this thread's bins: top, top-1, ...
+    unsigned own = 0;
+    for (int i = 0; i < per; ++i) own += hist[top - i];
+    const unsigned incl = block_scan_incl(own, warp_tot, nullptr);
+    const unsigned excl = incl - own;
+    if (excl < K && K <= incl) {
+        unsigned run = excl;
+        for (int i = 0; i < per; ++i) {
+            const unsigned c = hist[top - i];
+            if (run + c >= K) {
+                out->bin = top - i; out->above = run; out->in_bin = c;
+                break;
+            }
+            run += c;
+        }
+    }
+    __syncthreads();
+    const BinSplit r = *out;
+    __syncthreads();
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// block-wide radix select over one row (8-bit digits, MSB first) + ordered
+// emission of the kept positions into out[0 .. K-1]
+// ---------------------------------------------------------------------------
+struct RadixShared {
+    unsigned hist[RADIX];
+    unsigned warp_tot[32];
+    int digit, above, cnt;
+};
+
+// Finds d* with count(digit > d*) < need <= count(digit >= d*). Warp 0 only.
+SA_DEVINL void radix_find_digit(RadixShared& sh, unsigned need)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned own = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) own += sh.hist[255 - 8 * lane - i];
+    unsigned incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const unsigned excl = incl - own;
+    if (excl < need && need <= incl) {
+        unsigned run = excl;
+        for (int i = 0; i < 8; ++i) {
+            const int d = 255 - 8 * lane - i;
+            const unsigned c = sh.hist[d];
+            if (run + c >= need) {
+                sh.digit = d; sh.above = (int)run; sh.cnt = (int)c;
+                break;
+            }
+            run += c;
+        }
+    }
+}
+
+// MSB-first radix search over cnt values v[0..cnt) in shared memory (8-bit
+// digits): on return, the values v with (v & mask) >= prefix number at least
+// `need`, and exactly `need` when the values are distinct. Whole block.
+// `start_shift` is the lowest bit of the first digit examined: callers that
+// know the values share their top bits start below them (and must then merge
+// those bits into prefix and mask themselves).
+template <typename T>
+__device__ void radix_kth(const T* v, unsigned cnt, unsigned need, RadixShared& sh, T& prefix_out, T& mask_out,
+                          int start_shift = (int)sizeof(T) * 8 - 8)
+{
+    const int tid = threadIdx.x, nth = blockDim.x;
+    T prefix = 0, mask = 0;
+    for (int shift = start_shift; shift >= 0; shift -= 8) {
+        for (int i = tid; i < RADIX; i += nth) sh.hist[i] = 0;
+        __syncthreads();
+        for (unsigned i = tid; i < cnt; i += nth) {
+            const T x = v[i];
+            if ((x & mask) == prefix) atomicAdd(&sh.hist[(unsigned)(x >> shift) & (RADIX - 1)], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) radix_find_digit(sh, need);
+        __syncthreads();
+        prefix |= (T)sh.digit << shift;
+        mask |= (T)(RADIX - 1) << shift;
+        need -= (unsigned)sh.above;
+        const bool done = need == (unsigned)sh.cnt;     // the whole bucket is kept
+        __syncthreads();
+        if (done) break;
+    }
+    prefix_out = prefix;
+    mask_out = mask;
+}
+
+// Keeps the K best of the n keys given by key_at(j) (n > K) and writes their
+// positions in ascending order to out[0 .. K-1]. Whole block, blockDim.x a
+// multiple of 32.
+template <typename KeyAt>
+__device__ void radix_select_row(KeyAt key_at, int64_t n, int K, int32_t* out, RadixShared& sh)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nth = blockDim.x;
+    uint32_t prefix = 0, mask = 0;
+    unsigned need = (unsigned)K;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < RADIX; i += nth) sh.hist[i] = 0;
+        __syncthreads();
+        for (int64_t j = tid; j < n; j += nth) {
+            const uint32_t u = key_at(j);
+            if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & (RADIX - 1)], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) radix_find_digit(sh, need);
+        __syncthreads();
+        prefix |= (uint32_t)sh.digit << shift;
+        mask |= (uint32_t)(RADIX - 1) << shift;
+        need -= (unsigned)sh.above;
+        const bool done = need == (unsigned)sh.cnt;   // the whole bucket is kept
+        __syncthreads();
+        if (done) break;
+    }
+
+    // ordered emission: keys above the threshold, plus the first `need`
+    // (lowest positions) of those equal to it
+    const uint32_t lanemask_lt = (1u << lane) - 1u;
+    unsigned written = 0, eq_before = 0;
+    for (int64_t j0 = 0; j0 < n; j0 += nth) {
+        const int64_t j = j0 + tid;
+        bool gt = false, eq = false;
+        if (j < n) {
+            const uint32_t u = key_at(j) & mask;
+            gt = u > prefix;
+            eq = u == prefix;
+        }
+        const unsigned bgt = __ballot_sync(0xffffffffu, gt);
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) sh.warp_tot[warp] = __popc(bgt) | (__popc(beq) << 16);
+        __syncthreads();
+        unsigned wpre = 0, tot = 0;
+        for (int w = 0; w < (nth >> 5); ++w) {
+            const unsigned v = sh.warp_tot[w];
+            wpre += (w < warp) ? v : 0u;
+            tot += v;
+        }
+        const unsigned gt_ex = (wpre & 0xffff) + __popc(bgt & lanemask_lt);
+        const unsigned eq_ex = (wpre >> 16) + __popc(beq & lanemask_lt);
+        const unsigned eq_quota = need > eq_before ? need - eq_before : 0u;
+        if (gt || (eq && eq_ex < eq_quota)) {
+            const unsigned pos = written + gt_ex + min(eq_ex, eq_quota);
+            if (pos < (unsigned)K) out[pos] = (int32_t)j;
+        }
+        written += (tot & 0xffff) + min(tot >> 16, eq_quota);
+        eq_before += tot >> 16;
+        __syncthreads();
+    }
+}
+
+}  // namespace sa

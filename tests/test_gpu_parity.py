@@ -252,3 +252,70 @@ def test_decode_latent_row_given_as_separate_value_copy(sa):
                                 1 / math.sqrt(cfg.dqk), dv=cfg.dv, idx_out=idx)
     torch.cuda.synchronize()
     _check_decode(cfg, inp, to_host(out), to_host(idx).numpy())
+
+
+# ---------------------------------------------------------------------------
+# tensor-core indexer over many tiles and work items (pipeline wrap-around)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,Hi,di", [(torch.bfloat16, 4, 64), (torch.float8_e4m3fn, 8, 64),
+                                         (torch.bfloat16, 16, 32), (torch.float8_e4m3fn, 4, 128)])
+def test_indexer_score_many_tiles(sa, dtype, Hi, di):
+    T, N = 1500, 2600
+    q, qs, w, k, ks = _indexer_inputs(T, N, Hi, di, dtype, seed=77 + Hi + di)
+    dq = lambda x: None if x is None else x.to(DEV)
+    off = N - T                                   # the last query sees every key
+    got = to_host(sa.indexer_score(dq(q), dq(w), dq(k), dq(qs), dq(ks), causal_offset=off)).double().numpy()
+    rows = np.arange(T)
+    n = np.clip(rows + 1 + off, 0, N)
+    ref = oracle.indexer(q, w, k, rows, np.zeros(T), n, qs, ks)
+    den = score_denominators(q, w, k, rows, np.zeros(T), n, qs, ks)
+    for t in range(T):
+        check_scores(got[t, :n[t]], ref[t], den[t], RTOL_SCORE[dtype], f"t={t}")
+        assert np.isnan(got[t, n[t]:]).all()
+
+
+# ---------------------------------------------------------------------------
+# decode Top-K paths: the whole threshold bin kept, and a bin too full for
+# the candidate list (exact radix select over the row)
+# ---------------------------------------------------------------------------
+
+def _decode_with_indexer(sa, ctx_list, K, k_sign_fn, seed):
+    cfg = get_config("decode_ragged", B=len(ctx_list), ctx_range=(), ctx_list=tuple(ctx_list), K=K)
+    inp = make_decode(cfg, seed=seed)
+    ntot = inp["total_rows"]
+    e0 = torch.zeros(cfg.di)
+    e0[0] = 1.0
+    sign = torch.as_tensor(k_sign_fn(ntot), dtype=torch.float32)
+    inp["k_idx_cache"] = (sign[:, None] * e0[None, :]).to(torch.bfloat16)
+    inp["q_idx"] = e0.expand(cfg.B, cfg.Hi, cfg.di).contiguous().to(torch.bfloat16)
+    out, idx = _run_decode(sa, cfg, inp)
+    _check_decode(cfg, inp, out, idx)
+    return cfg, inp, idx
+
+
+def test_decode_topk_exactly_k_in_top_bin(sa):
+    # scores are 1 at exactly K positions of each sequence and 0 elsewhere
+    rng = np.random.default_rng(3)
+    lens = [9000, 20000]
+    K = 300
+    sign = np.full(sum(lens), -1.0)
+    keep = []
+    start = 0
+    for n in lens:
+        pos = np.sort(rng.choice(n, size=K, replace=False))
+        sign[start + pos] = 1.0
+        keep.append(pos)
+        start += n
+    _, _, idx = _decode_with_indexer(sa, lens, K, lambda n: sign, seed=41)
+    for b in range(len(lens)):
+        assert np.array_equal(idx[b], keep[b])
+
+
+def test_decode_topk_all_scores_tied(sa):
+    # every score is exactly 0: the K lowest positions win (too many ties for
+    # the candidate list, so the row takes the full radix select)
+    lens = [40000, 3000, 2048]
+    _, _, idx = _decode_with_indexer(sa, lens, 2048, lambda n: -np.ones(n), seed=42)
+    for b, n in enumerate(lens):
+        assert np.array_equal(idx[b], np.arange(2048))
