@@ -1,297 +1,266 @@
-// Exact attention over the kept rows, warp-specialized, for MQA heads of
-// width 64 or 128 ("Hybrid Attention Architectures...", section 3.1, exact
-// computation stage over the candidate set; the sigmoid output gate of the
-// section 3.3 pseudocode is applied in the epilogue). The pages name the
-// gather of non-contiguous rows as the operator to get right ("Hybrid
-// Attention Architectures...", section 5, item 1).
+// Exact attention over the kept rows, for MQA heads of width 64 or 128
+// ("Hybrid Attention Architectures...", section 3.1, exact computation stage
+// over the candidate set; the sigmoid output gate of the section 3.3
+// pseudocode is applied in the epilogue). The pages name the gather of
+// non-contiguous rows as the operator to get right (same page, section 5,
+// item 1).
 //
 // One CTA per (query row, split of its kept rows, group of 16 heads). The 16
 // heads of a token share every gathered K/V row (one KV head), so a row is
-// fetched once for all of them.
-//   warp 0     producer: for each stage of 64 kept rows it reads the 64
-//              positions, then copies every K and V row with 16-byte
-//              cp.async (one warp instruction per row for 128-wide heads:
-//              half the lanes copy the key, half the value) into padded
-//              shared-memory rows, and has the stage's mbarrier count the
-//              copies as they land (cp.async.mbarrier.arrive); three stages
-//              in flight.
-//   warps 1-4  consumers: warp w owns rows 16w..16w+15 of every stage and
-//              keeps its own online softmax (running max, sum, 16 x dv fp32
-//              accumulator) over the rows it sees, so no barrier is needed per
-//              stage: S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 ->
-//              fp32), with P passed from the S accumulators straight into the
-//              A fragments. The running max is raised only when a new score
-//              exceeds it by more than 2^8 in the exp2 domain (the result does
-//              not depend on when it is raised; this only skips rescales).
+// fetched once for all of them. The four warps work independently: warp w
+// takes the 16-row steps w, w + 4, w + 8, ... of the CTA's kept rows, copies
+// each step's K and V rows with 16-byte cp.async into its own three-stage
+// ring of padded shared-memory rows (one warp instruction per row: half the
+// lanes copy the key, half the value), and keeps its own online softmax
+// (running max, sum, 16 x dv fp32 accumulator) over the rows it sees. Every
+// warp thus keeps its own loads in flight, and no barrier is needed until
+// the end. S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 -> fp32),
+// P passing from the S accumulators straight into the A fragments. The
+// running max is raised only when a new score exceeds it by more than 2^8 in
+// the exp2 domain (the result does not depend on when it is raised; this only
+// skips rescales).
 // At the end the four warps' (max, sum, accumulator) triples are merged in
 // shared memory; with one split the gate is applied and bf16 rows written,
 // with several splits the partials go to the workspace and the last CTA of
-// the row (atomic ticket) merges them. Every mbarrier wait is bounded.
+// the row (atomic ticket) merges them.
 #include "attn_common.cuh"
-#include "tc.cuh"
 #include "../../include/sparse_attn.h"
 
 namespace sa {
-
-// error word of the bounded waits (read back by sa_device_errors)
-__device__ unsigned g_attn_error = 0;
-
 namespace {
 
-constexpr int GA_CW = 4;                       // consumer warps
-constexpr int GA_THREADS = 32 * (GA_CW + 1);
-constexpr int GA_CH = 16 * GA_CW;              // kept rows per stage
-constexpr int GA_STAGES = 3;
+constexpr int GA_W = 4;                        // warps per CTA
+constexpr int GA_THREADS = 32 * GA_W;
+constexpr int GA_ROWS = 16;                    // kept rows per warp step (the MMA key tile)
+constexpr int GA_STAGES = 3;                   // per-warp pipeline depth
 constexpr float GA_RESCALE = 8.0f;             // lazy-rescale margin (exp2 domain)
 
 template <int DQK, int DV>
 struct GaCfg {
     static constexpr int K_LD = DQK + 8, V_LD = DV + 8;       // padded rows (bf16 elements)
-    static constexpr int KBYTES = GA_CH * K_LD * 2;
-    static constexpr int STAGE = KBYTES + GA_CH * V_LD * 2;
-    static constexpr int PK = DQK / 8, PV = DV / 8;           // 16-byte pieces per row
-    static constexpr int ROWS_PER_STEP = 32 / (PK + PV);      // rows copied per warp instruction
+    static constexpr int KBYTES = GA_ROWS * K_LD * 2;         // K part of one warp stage
+    static constexpr int WSTAGE = KBYTES + GA_ROWS * V_LD * 2;
+    static constexpr int WRING = GA_STAGES * WSTAGE;          // one warp's ring
     static constexpr int Q_LD = DQK + 8;
-    static constexpr int OFF_Q = GA_STAGES * STAGE;
-    static constexpr int OFF_BAR = (OFF_Q + 16 * Q_LD * 2 + 15) / 16 * 16;
-    static constexpr int SMEM = OFF_BAR + 8 * 2 * GA_STAGES + 128;
-    static_assert(32 % (PK + PV) == 0, "a row's pieces must tile the warp");
-    static_assert(4 * 16 * DV * 4 + 2 * 4 * 16 * 4 <= GA_STAGES * STAGE, "merge scratch fits the stages");
+    static constexpr int OFF_Q = GA_W * WRING;
+    static constexpr int SMEM = OFF_Q + 16 * Q_LD * 2;
+    static constexpr int PK = DQK / 8;                        // 16-byte pieces of a key row
+    static constexpr int PR = DQK / 8 + DV / 8;               // pieces of a key row + value row
+    static constexpr int RPI = 32 / PR;                       // rows per copy instruction
+    static_assert(PR == 32 || PR == 16, "one or two rows per warp instruction");
+    static_assert(4 * 16 * DV * 4 + 2 * 4 * 16 * 4 <= OFF_Q, "merge scratch fits the rings");
 };
-
-SA_DEVINL void cp_async_arrive_noinc(uint64_t* bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
-}
 
 template <int DQK, int DV>
 __global__ void __launch_bounds__(GA_THREADS, 2)
 attn_gather_kernel(AttnArgs a)
 {
     using C = GaCfg<DQK, DV>;
-    extern __shared__ uint8_t ga_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ga_raw) + 127) & ~uintptr_t(127));
+    extern __shared__ __align__(16) uint8_t smem[];
     bf16* Qs = reinterpret_cast<bf16*>(smem + C::OFF_Q);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* empty = full + GA_STAGES;
     __shared__ int sh_flag;
 
     griddep_wait();                          // the kept positions
     griddep_launch();
     const int r = blockIdx.x, split = blockIdx.y, hg = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3, mat = lane >> 3, rr = lane & 7;
     const int64_t n = attn_hist_len(a, r);
     const int n_sel = (int)min64(a.K, n);
     const int per = (a.K + a.splits - 1) / a.splits;
     const int begin = min(split * per, n_sel), end = min(begin + per, n_sel);
     const int cnt = end - begin;
-    const int nchunks = (cnt + GA_CH - 1) / GA_CH;
+    const int nsteps = (cnt + GA_ROWS - 1) / GA_ROWS;
+    const int my_steps = nsteps > warp ? (nsteps - warp + GA_W - 1) / GA_W : 0;
     const int64_t base = attn_base(a, r);
     const int32_t* sel = a.idx + (int64_t)r * a.K;
+    const int fallback = cnt > 0 ? sel[begin] : 0;      // a kept position: always a valid row
 
-    if (threadIdx.x == 0) {
-        // full: one arrival per producer lane (its copies landed); empty: one per consumer warp
-        for (int s = 0; s < GA_STAGES; ++s) { mbar_init(&full[s], 32); mbar_init(&empty[s], GA_CW); }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    float o[DV / 8][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    const int g = lane >> 2, t4 = lane & 3, mat = lane >> 3, rr = lane & 7;
-    const int cw = warp - 1;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (nchunks > 0) {
-            const int fallback = sel[begin];                 // a kept position, always valid
-            const int piece = lane % (C::PK + C::PV), sub = lane / (C::PK + C::PV);
-            const bool is_k = piece < C::PK;
-            const bf16* src_base = is_k ? static_cast<const bf16*>(a.k) + piece * 8
-                                        : static_cast<const bf16*>(a.v) + (piece - C::PK) * 8;
-            const int64_t ld = is_k ? a.ld_k : a.ld_v;
-            const int dst_off = is_k ? piece * 8 : C::KBYTES / 2 + (piece - C::PK) * 8;
-            const int dst_ld = is_k ? C::K_LD : C::V_LD;
-            // positions of stage c: slots begin + c*64 + lane and + 32; loaded one
-            // stage ahead so that their latency hides behind the copies
-            auto load_pos = [&](int c, int (&pos)[2]) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int slot = begin + c * GA_CH + lane + 32 * h;
-                    pos[h] = slot < end ? sel[slot] : fallback;
-                }
-            };
-            int nxt[2];
-            load_pos(0, nxt);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % GA_STAGES;
-                const uint32_t ph = (uint32_t)(c / GA_STAGES) & 1u;
-                int cur[2] = {nxt[0], nxt[1]};
-                if (c + 1 < nchunks) load_pos(c + 1, nxt);
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, &g_attn_error);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                int64_t rows[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int pos = (cur[h] < 0 || cur[h] >= n) ? fallback : cur[h];
-                    rows[h] = base + pos;
-                }
-                bf16* dst = reinterpret_cast<bf16*>(smem + s * C::STAGE) + dst_off;
-#pragma unroll 4
-                for (int r0 = 0; r0 < GA_CH; r0 += C::ROWS_PER_STEP) {
-                    const int rrow = r0 + sub;
-                    const int64_t lo = __shfl_sync(0xffffffffu, rows[0], rrow & 31);
-                    const int64_t hi = __shfl_sync(0xffffffffu, rows[1], rrow & 31);
-                    const int64_t grow = (rrow >> 5) ? hi : lo;
-                    cp_async16(dst + rrow * dst_ld, src_base + grow * ld, true);
-                }
-                cp_async_arrive_noinc(&full[s]);             // counts once this lane's copies land
-            }
-            // do not leave with copies in flight: wait (bounded) for the last stages
-            if (lane == 0) {
-                for (int c = max(0, nchunks - GA_STAGES); c < nchunks; ++c)
-                    (void)mbar_wait(&full[c % GA_STAGES], (uint32_t)(c / GA_STAGES) & 1u, &g_attn_error);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
-        // Q tile: 16 heads of this group
+    // Q tile: 16 heads of this group
+    {
         const bf16* q = static_cast<const bf16*>(a.q);
-        for (int i = threadIdx.x - 32; i < 16 * (DQK / 8); i += 32 * GA_CW) {
+        for (int i = threadIdx.x; i < 16 * (DQK / 8); i += GA_THREADS) {
             const int row = i / (DQK / 8), pc = i % (DQK / 8), h = hg * 16 + row;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (h < a.Hq) v = *reinterpret_cast<const uint4*>(q + ((int64_t)r * a.Hq + h) * DQK + pc * 8);
             *reinterpret_cast<uint4*>(Qs + row * C::Q_LD + pc * 8) = v;
         }
-        asm volatile("bar.sync 1, %0;" :: "r"(32 * GA_CW) : "memory");
-#pragma unroll
-        for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-        const float sl2 = a.softmax_scale * LOG2E;
-        const uint32_t qbase = smem_u32(Qs);
-        bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int s = c % GA_STAGES;
-            ok = mbar_wait(&full[s], (uint32_t)(c / GA_STAGES) & 1u, &g_attn_error);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const uint32_t st = smem_u32(smem + s * C::STAGE);
-            const uint32_t vst = st + C::KBYTES;
-            // S = Q K^T for this warp's 16 rows (keys)
-            float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-#pragma unroll
-            for (int ks = 0; ks < DQK / 16; ++ks) {
-                uint32_t af[4], bfm[4];
-                ldsm_x4(af, qbase + (uint32_t)((((mat & 1) * 8 + rr) * C::Q_LD + ks * 16 + (mat >> 1) * 8) * 2));
-                const int krow = cw * 16 + (mat >> 1) * 8 + rr;
-                const int dim = ks * 16 + (mat & 1) * 8;
-                ldsm_x4(bfm, st + (uint32_t)((krow * C::K_LD + dim) * 2));
-                mma_16816(sc[0], af, bfm[0], bfm[1]);
-                mma_16816(sc[1], af, bfm[2], bfm[3]);
-            }
-            // mask slots past the end, scale to the exp2 domain
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const bool valid = begin + c * GA_CH + cw * 16 + nt * 8 + 2 * t4 + e < end;
-                    sc[nt][e] = valid ? sc[nt][e] * sl2 : -INFINITY;
-                    sc[nt][2 + e] = valid ? sc[nt][2 + e] * sl2 : -INFINITY;
-                    mx0 = fmaxf(mx0, sc[nt][e]);
-                    mx1 = fmaxf(mx1, sc[nt][2 + e]);
-                }
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const bool up0 = mx0 > m0 + GA_RESCALE, up1 = mx1 > m1 + GA_RESCALE;
-            if (__any_sync(0xffffffffu, up0 || up1)) {
-                float a0 = 1.0f, a1 = 1.0f;
-                if (up0) { a0 = (m0 == -INFINITY) ? 0.0f : exp2f(m0 - mx0); m0 = mx0; }
-                if (up1) { a1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - mx1); m1 = mx1; }
-                l0 *= a0;
-                l1 *= a1;
-#pragma unroll
-                for (int i = 0; i < DV / 8; ++i) {
-                    o[i][0] *= a0; o[i][1] *= a0; o[i][2] *= a1; o[i][3] *= a1;
-                }
-            }
-            const float ref0 = (m0 == -INFINITY) ? 0.0f : m0, ref1 = (m1 == -INFINITY) ? 0.0f : m1;
-            uint32_t pa[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t p01 = pack_bf16x2(exp2f(sc[nt][0] - ref0), exp2f(sc[nt][1] - ref0));
-                const uint32_t p23 = pack_bf16x2(exp2f(sc[nt][2] - ref1), exp2f(sc[nt][3] - ref1));
-                const float2 f01 = bf16x2_to_f32x2(p01), f23 = bf16x2_to_f32x2(p23);
-                l0 += f01.x + f01.y;
-                l1 += f23.x + f23.y;
-                pa[2 * nt] = p01;
-                pa[2 * nt + 1] = p23;
-            }
-            // O += P V over this warp's 16 rows
-#pragma unroll
-            for (int np = 0; np < DV / 16; ++np) {
-                uint32_t bfm[4];
-                const int vrow = cw * 16 + (mat & 1) * 8 + rr;
-                const int col = np * 16 + (mat >> 1) * 8;
-                ldsm_x4_trans(bfm, vst + (uint32_t)((vrow * C::V_LD + col) * 2));
-                mma_16816(o[2 * np], pa, bfm[0], bfm[1]);
-                mma_16816(o[2 * np + 1], pa, bfm[2], bfm[3]);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    }
 
-        // merge the four warps' partial triples (stage memory is free now)
-        asm volatile("bar.sync 1, %0;" :: "r"(32 * GA_CW) : "memory");
-        float* Ow = reinterpret_cast<float*>(smem);               // [4][16][DV]
-        float* mw = Ow + 4 * 16 * DV;                             // [4][16]
-        float* lw = mw + 4 * 16;                                  // [4][16]
-#pragma unroll
-        for (int i = 0; i < DV / 8; ++i) {
-            const int col = i * 8 + 2 * t4;
-            *reinterpret_cast<float2*>(&Ow[(cw * 16 + g) * DV + col]) = make_float2(o[i][0], o[i][1]);
-            *reinterpret_cast<float2*>(&Ow[(cw * 16 + g + 8) * DV + col]) = make_float2(o[i][2], o[i][3]);
+    // this warp's ring; step k of the warp is CTA step warp + 4k
+    uint8_t* ring = smem + warp * C::WRING;
+    const int piece = lane % C::PR, sub = lane / C::PR;
+    const bool is_k = piece < C::PK;
+    const bf16* src_base = is_k ? static_cast<const bf16*>(a.k) + piece * 8
+                                : static_cast<const bf16*>(a.v) + (piece - C::PK) * 8;
+    const int64_t src_ld = is_k ? a.ld_k : a.ld_v;
+    const int dst_ld = is_k ? C::K_LD : C::V_LD;
+    const int dst_off = is_k ? piece * 8 : C::KBYTES / 2 + (piece - C::PK) * 8;
+    // lanes 0..15 hold the positions of one step's 16 rows
+    auto load_pos = [&](int k) -> int {
+        int pos = fallback;
+        if (k < my_steps && lane < GA_ROWS) {
+            const int slot = begin + (warp + k * GA_W) * GA_ROWS + lane;
+            pos = slot < end ? sel[slot] : fallback;
+            if (pos < 0 || pos >= n) pos = fallback;
         }
-        if (t4 == 0) {
-            mw[cw * 16 + g] = m0; mw[cw * 16 + g + 8] = m1;
-            lw[cw * 16 + g] = l0; lw[cw * 16 + g + 8] = l1;
+        return pos;
+    };
+    auto issue = [&](int k, int pos) {
+        if (k < my_steps) {
+            const int64_t grow = base + pos;
+            bf16* dst = reinterpret_cast<bf16*>(ring + (k % GA_STAGES) * C::WSTAGE) + dst_off;
+#pragma unroll
+            for (int r0 = 0; r0 < GA_ROWS; r0 += C::RPI) {
+                const int rrow = r0 + sub;
+                const int64_t gr = __shfl_sync(0xffffffffu, grow, rrow);
+                cp_async16(dst + rrow * dst_ld, src_base + gr * src_ld, true);
+            }
         }
-        asm volatile("bar.sync 1, %0;" :: "r"(32 * GA_CW) : "memory");
-        const int ct = threadIdx.x - 32;
-        for (int e = ct; e < 16 * (DV / 2); e += 32 * GA_CW) {
-            const int hh = e / (DV / 2), col = 2 * (e % (DV / 2)), h = hg * 16 + hh;
-            if (h >= a.Hq) continue;
-            float M = -INFINITY;
+        cp_async_commit();                   // one group per step, empty past the end
+    };
+
+    int pos_next = load_pos(0);
 #pragma unroll
-            for (int w = 0; w < GA_CW; ++w) M = fmaxf(M, mw[w * 16 + hh]);
-            float L = 0.0f, O0 = 0.0f, O1 = 0.0f;
-            if (M != -INFINITY) {
+    for (int k = 0; k < GA_STAGES - 1; ++k) {
+        const int pos = pos_next;
+        pos_next = load_pos(k + 1);
+        issue(k, pos);
+    }
+    __syncthreads();                         // the Q tile
+
+    float o[DV / 8][4];
 #pragma unroll
-                for (int w = 0; w < GA_CW; ++w) {
-                    const float mwv = mw[w * 16 + hh];
-                    const float f = mwv == -INFINITY ? 0.0f : exp2f(mwv - M);
-                    L = fmaf(lw[w * 16 + hh], f, L);
-                    const float2 ov = *reinterpret_cast<const float2*>(&Ow[(w * 16 + hh) * DV + col]);
-                    O0 = fmaf(ov.x, f, O0);
-                    O1 = fmaf(ov.y, f, O1);
-                }
+    for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    const float sl2 = a.softmax_scale * LOG2E;
+    const uint32_t qbase = smem_u32(Qs);
+
+    for (int k = 0; k < my_steps; ++k) {
+        {
+            const int pos = pos_next;
+            pos_next = load_pos(k + GA_STAGES);
+            issue(k + GA_STAGES - 1, pos);
+        }
+        cp_async_wait<GA_STAGES - 1>();      // this lane's copies of step k have landed
+        __syncwarp();                        // ... and every lane's
+        const uint32_t st = smem_u32(ring + (k % GA_STAGES) * C::WSTAGE);
+        const uint32_t vst = st + C::KBYTES;
+        const int slot0 = begin + (warp + k * GA_W) * GA_ROWS;
+
+        // S = Q K^T for the step's 16 rows (keys)
+        float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+        for (int ks = 0; ks < DQK / 16; ++ks) {
+            uint32_t af[4], bfm[4];
+            ldsm_x4(af, qbase + (uint32_t)((((mat & 1) * 8 + rr) * C::Q_LD + ks * 16 + (mat >> 1) * 8) * 2));
+            const int krow = (mat >> 1) * 8 + rr;
+            const int dim = ks * 16 + (mat & 1) * 8;
+            ldsm_x4(bfm, st + (uint32_t)((krow * C::K_LD + dim) * 2));
+            mma_16816(sc[0], af, bfm[0], bfm[1]);
+            mma_16816(sc[1], af, bfm[2], bfm[3]);
+        }
+        // mask slots past the end, scale to the exp2 domain
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const bool valid = slot0 + nt * 8 + 2 * t4 + e < end;
+                sc[nt][e] = valid ? sc[nt][e] * sl2 : -INFINITY;
+                sc[nt][2 + e] = valid ? sc[nt][2 + e] * sl2 : -INFINITY;
+                mx0 = fmaxf(mx0, sc[nt][e]);
+                mx1 = fmaxf(mx1, sc[nt][2 + e]);
             }
-            if (a.splits == 1) {
-                const float gs = L > 0.0f ? gate_of(a, r, h) / L : 0.0f;
-                *reinterpret_cast<uint32_t*>(static_cast<bf16*>(a.out) + ((int64_t)r * a.Hq + h) * DV + col) =
-                    pack_bf16x2(O0 * gs, O1 * gs);
-            } else {
-                float* p = a.part + (((int64_t)r * a.splits + split) * a.Hq + h) * (DV + 2);
-                *reinterpret_cast<float2*>(p + col) = make_float2(O0, O1);
-                if (col == 0) { p[DV] = M; p[DV + 1] = L; }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const bool up0 = mx0 > m0 + GA_RESCALE, up1 = mx1 > m1 + GA_RESCALE;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+            float a0 = 1.0f, a1 = 1.0f;
+            if (up0) { a0 = (m0 == -INFINITY) ? 0.0f : exp2f(m0 - mx0); m0 = mx0; }
+            if (up1) { a1 = (m1 == -INFINITY) ? 0.0f : exp2f(m1 - mx1); m1 = mx1; }
+            l0 *= a0;
+            l1 *= a1;
+#pragma unroll
+            for (int i = 0; i < DV / 8; ++i) {
+                o[i][0] *= a0; o[i][1] *= a0; o[i][2] *= a1; o[i][3] *= a1;
             }
+        }
+        const float ref0 = (m0 == -INFINITY) ? 0.0f : m0, ref1 = (m1 == -INFINITY) ? 0.0f : m1;
+        uint32_t pa[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t p01 = pack_bf16x2(exp2f(sc[nt][0] - ref0), exp2f(sc[nt][1] - ref0));
+            const uint32_t p23 = pack_bf16x2(exp2f(sc[nt][2] - ref1), exp2f(sc[nt][3] - ref1));
+            const float2 f01 = bf16x2_to_f32x2(p01), f23 = bf16x2_to_f32x2(p23);
+            l0 += f01.x + f01.y;
+            l1 += f23.x + f23.y;
+            pa[2 * nt] = p01;
+            pa[2 * nt + 1] = p23;
+        }
+        // O += P V over the step's 16 rows
+#pragma unroll
+        for (int np = 0; np < DV / 16; ++np) {
+            uint32_t bfm[4];
+            const int vrow = (mat & 1) * 8 + rr;
+            const int col = np * 16 + (mat >> 1) * 8;
+            ldsm_x4_trans(bfm, vst + (uint32_t)((vrow * C::V_LD + col) * 2));
+            mma_16816(o[2 * np], pa, bfm[0], bfm[1]);
+            mma_16816(o[2 * np + 1], pa, bfm[2], bfm[3]);
+        }
+        __syncwarp();                        // the slot is refilled by the next issue
+    }
+    cp_async_wait<0>();
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    // merge the four warps' partial triples (the rings are free now)
+    __syncthreads();
+    float* Ow = reinterpret_cast<float*>(smem);                   // [4][16][DV]
+    float* mw = Ow + 4 * 16 * DV;                                 // [4][16]
+    float* lw = mw + 4 * 16;                                      // [4][16]
+#pragma unroll
+    for (int i = 0; i < DV / 8; ++i) {
+        const int col = i * 8 + 2 * t4;
+        *reinterpret_cast<float2*>(&Ow[(warp * 16 + g) * DV + col]) = make_float2(o[i][0], o[i][1]);
+        *reinterpret_cast<float2*>(&Ow[(warp * 16 + g + 8) * DV + col]) = make_float2(o[i][2], o[i][3]);
+    }
+    if (t4 == 0) {
+        mw[warp * 16 + g] = m0; mw[warp * 16 + g + 8] = m1;
+        lw[warp * 16 + g] = l0; lw[warp * 16 + g + 8] = l1;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < 16 * (DV / 2); e += GA_THREADS) {
+        const int hh = e / (DV / 2), col = 2 * (e % (DV / 2)), h = hg * 16 + hh;
+        if (h >= a.Hq) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < GA_W; ++w) M = fmaxf(M, mw[w * 16 + hh]);
+        float L = 0.0f, O0 = 0.0f, O1 = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < GA_W; ++w) {
+                const float mwv = mw[w * 16 + hh];
+                const float f = mwv == -INFINITY ? 0.0f : exp2f(mwv - M);
+                L = fmaf(lw[w * 16 + hh], f, L);
+                const float2 ov = *reinterpret_cast<const float2*>(&Ow[(w * 16 + hh) * DV + col]);
+                O0 = fmaf(ov.x, f, O0);
+                O1 = fmaf(ov.y, f, O1);
+            }
+        }
+        if (a.splits == 1) {
+            const float gs = L > 0.0f ? gate_of(a, r, h) / L : 0.0f;
+            *reinterpret_cast<uint32_t*>(static_cast<bf16*>(a.out) + ((int64_t)r * a.Hq + h) * DV + col) =
+                pack_bf16x2(O0 * gs, O1 * gs);
+        } else {
+            float* p = a.part + (((int64_t)r * a.splits + split) * a.Hq + h) * (DV + 2);
+            *reinterpret_cast<float2*>(p + col) = make_float2(O0, O1);
+            if (col == 0) { p[DV] = M; p[DV + 1] = L; }
         }
     }
 

@@ -30,7 +30,7 @@ namespace {
 
 constexpr int SCAN_THREADS = 256;           // 8 warps
 constexpr int SCAN_CHUNK = 4096;            // keys per CTA
-constexpr int scan_unroll(int di) { return di <= 64 ? 4 : (di == 128 ? 2 : 1); }   // 16-key groups in flight per warp
+__host__ __device__ constexpr int scan_unroll(int di) { return di <= 64 ? 4 : (di == 128 ? 2 : 1); }   // 16-key groups in flight per warp
 
 template <int DI, int NTH>
 __global__ void __launch_bounds__(SCAN_THREADS)

@@ -23,9 +23,9 @@
 //               ring of shared-memory stages (128-byte-swizzled K-major tiles)
 //   warp 1      TMEM owner (512 columns = two 128x256 fp32 accumulators) and
 //               MMA issuer (one thread, kind::f16 or kind::f8f6f4)
-//   warps 2-9   epilogue: TMEM -> registers, ReLU, weighted head sum, causal
-//               mask, fp32 store; two warps per TMEM sub-partition, each
-//               taking half of the 256 columns
+//   warps 2-17  epilogue: TMEM -> registers, ReLU, weighted head sum, causal
+//               mask, fp32 store; four warps per TMEM sub-partition, each
+//               taking a quarter of the 256 columns
 // Accumulators are double-buffered so that the epilogue of one key tile
 // overlaps the MMAs of the next. Every wait is bounded (see tc.cuh).
 #include <mutex>
@@ -45,8 +45,9 @@ namespace {
 constexpr int TC_BM = 128;                 // keys per tile (MMA M)
 constexpr int TC_BN = 256;                 // (query, head) pairs per tile (MMA N)
 constexpr int TC_GROUP = 8;                // key tiles per work item
-constexpr int TC_EPI_WARPS = 8;
+constexpr int TC_EPI_WARPS = 16;                          // four per TMEM sub-partition
 constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
+constexpr int TC_EPI_COLS = TC_BN * 4 / TC_EPI_WARPS;     // accumulator columns per epilogue thread
 
 template <int ES, int DI, int HI>
 struct TcCfg {
@@ -126,35 +127,34 @@ SA_DEVINL float head_sum(const uint32_t* r, const float* w)
     }
 }
 
-// Epilogue of one accumulator tile for one thread: its key's 128 columns
-// (128 / HI queries), read from TMEM 64 columns at a time; the accumulator is
-// released as soon as the last columns are in registers. FULL tiles lie inside
-// every query's causal window; the others test each (query, key) pair:
-// store iff t < T, j < N and j <= t + off.
+// Epilogue of one accumulator tile for one thread: TC_EPI_COLS columns of its
+// key (TC_EPI_COLS / HI queries), read from TMEM 32 columns at a time; the
+// accumulator is released as soon as the last columns are in registers. FULL
+// tiles lie inside every query's causal window; the others test each
+// (query, key) pair: store iff t < T, j < N and j <= t + off.
 template <int HI, bool FULL, bool FP8>
 SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int64_t ld_s, int64_t j,
                         int t_first, int T, int64_t off, uint64_t* empty_bar, int64_t N = 0)
 {
-    constexpr int QPH = 64 / HI;                       // queries per 64 columns
+    constexpr int QPC = 32 / HI;                       // queries per 32 columns
+    constexpr int CH = TC_EPI_COLS / 32;
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(taddr + hc * 64, ra);
-        tmem_ld32(taddr + hc * 64 + 32, rb);
+    for (int c = 0; c < CH; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
         tmem_ld_wait();
-        if (hc == 1) {
+        if (c == CH - 1) {
             tc_fence_before();
             mbar_arrive(empty_bar);
         }
 #pragma unroll
-        for (int qq = 0; qq < QPH; ++qq) {
-            const uint32_t* r = qq < QPH / 2 ? &ra[qq * HI] : &rb[(qq - QPH / 2) * HI];
-            float s = head_sum<HI>(r, w + (hc * QPH + qq) * HI);
+        for (int qq = 0; qq < QPC; ++qq) {
+            float s = head_sum<HI>(&r[qq * HI], w + (c * QPC + qq) * HI);
             if (FP8) s *= ks;
             if (FULL) {
                 *p = s;
             } else {
-                const int t = t_first + hc * QPH + qq;
+                const int t = t_first + c * QPC + qq;
                 if (t < T && j < N && j <= (int64_t)t + off) *p = s;
             }
             p += ld_s;
@@ -274,9 +274,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int e = threadIdx.x - 64;                 // 0 .. 255
+        const int e = threadIdx.x - 64;                 // 0 .. 32 * TC_EPI_WARPS - 1
         const int sub = warp & 3;                       // TMEM sub-partition of this warp
-        const int half = (warp - 2) >> 2;               // which 128 columns
+        const int half = (warp - 2) >> 2;               // which TC_EPI_COLS columns
         const int row = sub * 32 + lane;                // TMEM lane = key within the tile
         const bool fp8 = (ES == 1);
         int ab = 0;
@@ -305,7 +305,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             // skip the per-query causal mask
             const int64_t n_first = min64(a.N, max64(0, (int64_t)t0 + 1 + a.causal_offset));
             const bool rows_full = t0 + TQ <= a.T;
-            const int tq_first = half * (128 / HI);
+            const int tq_first = half * (TC_EPI_COLS / HI);
             for (int kt = k_begin; kt < k_end; ++kt) {
                 const int64_t j = (int64_t)kt * TC_BM + row;
                 const float ks = (fp8 && j < a.N) ? a.k_scale[j] : 1.0f;
@@ -314,7 +314,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) continue;
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * 128);
+                const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * TC_EPI_COLS);
                 float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
                 const float* w_half = sW + tq_first * HI;
                 if (full)
