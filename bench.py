@@ -5,8 +5,9 @@ One step = one sparse_attn_decode call for a batch of 32 sequences, each with
 131072 cached rows: indexer scan over every cached indexer key, exact Top-K
 (K=2048), gathered attention over the kept rows with the sigmoid gate, split-K
 combine. Prints one JSON line (rank 0). Also reports, in the same line, the
-prefill throughput of the 8K workload, the dominant kernel's roofline, an
-end-to-end number through host buffers, and the fp64 oracle timed on the host.
+prefill throughput of the 8K and 128K workloads with the tensor-core rate of
+their indexers, the dominant kernel's roofline, an end-to-end number through
+host buffers, and the fp64 oracle timed on the host.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -274,10 +275,45 @@ def workload_config(cfg):
 # our arm
 # ---------------------------------------------------------------------------
 
-def bench_prefill(sa, torch, dev, seed, iters=10):
-    """Prefill tok/s of the 8K workload, plus the standalone indexer's tensor rate."""
+def indexer_roofline(sa, torch, dev, cfg, inp, iters):
+    """The tensor-core indexer alone over every causal row of the workload, in
+    the same <= 1 GiB row passes the prefill uses; FLOPs = 2*Hi*di per causal
+    (query, key) pair."""
+    L = cfg.L
+    rows = max(1, min(L, (1 << 30) // (4 * ((L + 3) // 4 * 4))))
+    ld = (L + 3) // 4 * 4
+    scores = torch.empty((rows, ld), dtype=torch.float32, device=dev)
+
+    def sweep():
+        for t0 in range(0, L, rows):
+            t1 = min(L, t0 + rows)
+            qs = None if inp["q_scale"] is None else inp["q_scale"][t0:t1]
+            sa.indexer_score(inp["q_idx"][t0:t1], inp["w"][t0:t1], inp["k_idx"], qs, inp["k_scale"],
+                             causal_offset=t0, scores=scores[: t1 - t0])
+    sweep()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        sweep()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    flops = 2 * cfg.Hi * cfg.di * (L * (L + 1) // 2)
+    peaks = measured_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    del scores
+    return {"kernel": "indexer_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+            "peak_source": peaks["source"] + " burst bf16 (the north-star reference for both dtypes)",
+            "algorithmic_flops": flops, "ms": ms, "dtype": str(inp["q_idx"].dtype).replace("torch.", "")}
+
+
+def bench_prefill(sa, torch, dev, seed, name, iters):
+    """Prefill tok/s of one workload (stage split by events), plus the tensor
+    rate of its indexer."""
     from workloads import get_config, make_prefill
-    cfg = get_config(PREFILL_WORKLOAD)
+    cfg = get_config(name)
     inp = make_prefill(cfg, seed=seed, device=dev)
     scale = 1 / math.sqrt(cfg.dqk)
     out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
@@ -288,10 +324,9 @@ def bench_prefill(sa, torch, dev, seed, iters=10):
         if e is not None:
             e[0].record()
         sa.sparse_attn_prefill(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], inp["w"],
-                               inp["gate"], cfg.K, scale, out=out, idx_out=idx,
-                               stage_events=None if e is None else e[1:])
-    for _ in range(3):
-        step()
+                               inp["gate"], cfg.K, scale, q_scale=inp["q_scale"], k_scale=inp["k_scale"],
+                               out=out, idx_out=idx, stage_events=None if e is None else e[1:])
+    step()
     torch.cuda.synchronize()
     for i in range(iters):
         step(ev[i])
@@ -299,28 +334,11 @@ def bench_prefill(sa, torch, dev, seed, iters=10):
     tot = [ev[i][0].elapsed_time(ev[i][2]) for i in range(iters)]
     sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(iters)]
     ms = statistics.median(tot)
-    # standalone indexer (all causal rows), for its tensor-core rate
-    scores = torch.empty((cfg.L, cfg.L), dtype=torch.float32, device=dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(3):
-        sa.indexer_score(inp["q_idx"], inp["w"], inp["k_idx"], scores=scores)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(iters):
-        sa.indexer_score(inp["q_idx"], inp["w"], inp["k_idx"], scores=scores)
-    e1.record()
-    torch.cuda.synchronize()
-    ix_ms = e0.elapsed_time(e1) / iters
-    pairs = cfg.L * (cfg.L + 1) // 2
-    flops = 2 * cfg.Hi * cfg.di * pairs
-    peaks = measured_peaks()
-    ix_tflops = flops / (ix_ms * 1e-3) / 1e12
-    del scores
+    del out, idx
+    roof = indexer_roofline(sa, torch, dev, cfg, inp, iters)
     return {"workload": cfg.name, "L": cfg.L, "K": cfg.K, "tok_s": cfg.L / (ms * 1e-3), "ms": ms,
             "selection_ms": statistics.median(sel), "attention_ms": ms - statistics.median(sel),
-            "indexer_ms": ix_ms, "indexer_tflops": ix_tflops,
-            "indexer_frac_of_bf16_peak": ix_tflops / peaks["bf16_tflops"],
-            "indexer_peak_source": peaks["source"] + " burst bf16"}
+            "indexer_roofline": roof}
 
 
 def run_ours(args):
@@ -426,8 +444,10 @@ def run_ours(args):
 
     prefill = None
     if not args.no_prefill:
-        del host
-        prefill = bench_prefill(sa, torch, dev, args.seed + rank)
+        del host, inp
+        torch.cuda.empty_cache()
+        prefill = [bench_prefill(sa, torch, dev, args.seed + rank, PREFILL_WORKLOAD, 10),
+                   bench_prefill(sa, torch, dev, args.seed + rank, "prefill_128k", 2)]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -33,6 +33,7 @@ int check_indexer_shape(int dtype, int Hi, int di)
 // ---- prefill workspace layout --------------------------------------------
 struct PrefillLayout {
     int64_t rows_per_pass;   // query rows scored per indexer/Top-K pass
+    int64_t ld_s;            // score row stride: L rounded up to a multiple of 4 (16-byte rows)
     size_t idx_off, scores_off, total;
 };
 
@@ -41,14 +42,15 @@ PrefillLayout prefill_layout(const sa_prefill_args& a)
     PrefillLayout l{};
     const int64_t L = a.L;
     const int64_t budget = int64_t(1) << 30;               // bytes of scores per pass
-    int64_t rows = budget / (4 * (L > 0 ? L : 1));
+    l.ld_s = (L + 3) / 4 * 4;
+    int64_t rows = budget / (4 * (l.ld_s > 0 ? l.ld_s : 4));
     rows = rows < 1 ? 1 : (rows > L ? L : rows);
     l.rows_per_pass = rows;
     size_t off = 0;
     l.idx_off = off;
     if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * (size_t)L * a.K);
     l.scores_off = off;
-    off += align_up(sizeof(float) * (size_t)rows * (size_t)L);
+    off += align_up(sizeof(float) * (size_t)rows * (size_t)l.ld_s);
     l.total = off;
     return l;
 }
@@ -237,11 +239,11 @@ int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, 
         ia.q_idx = a.q_idx; ia.dtype = a.idx_dtype; ia.q_scale = a.q_scale; ia.w = a.w;
         ia.k_idx = a.k_idx; ia.k_scale = a.k_scale;
         ia.T = (int)t1; ia.N = (int)t1; ia.Hi = a.Hi; ia.di = a.di; ia.causal_offset = 0;
-        ia.t_begin = (int)t0; ia.scores = scores; ia.ld_s = a.L;
+        ia.t_begin = (int)t0; ia.scores = scores; ia.ld_s = lay.ld_s;
         cudaError_t e = sa::launch_indexer(ia, stream);
         if (e != cudaSuccess) return SA_ERR_LAUNCH;
         sa::TopkArgs ta{};
-        ta.scores = scores; ta.ld_s = a.L; ta.row_len = nullptr; ta.causal_first = t0;
+        ta.scores = scores; ta.ld_s = lay.ld_s; ta.row_len = nullptr; ta.causal_first = t0;
         ta.n_cap = a.L; ta.rows = (int)(t1 - t0); ta.K = a.K; ta.idx = idx + t0 * a.K; ta.ld_idx = a.K;
         e = sa::launch_topk(ta, stream);
         if (e != cudaSuccess) return SA_ERR_LAUNCH;

@@ -32,10 +32,9 @@ namespace {
 constexpr int GA_W = 4;                        // warps per CTA
 constexpr int GA_THREADS = 32 * GA_W;
 constexpr int GA_ROWS = 16;                    // kept rows per warp step (the MMA key tile)
-constexpr int GA_STAGES = 3;                   // per-warp pipeline depth
 constexpr float GA_RESCALE = 8.0f;             // lazy-rescale margin (exp2 domain)
 
-template <int DQK, int DV>
+template <int DQK, int DV, int GA_STAGES>
 struct GaCfg {
     static constexpr int K_LD = DQK + 8, V_LD = DV + 8;       // padded rows (bf16 elements)
     static constexpr int KBYTES = GA_ROWS * K_LD * 2;         // K part of one warp stage
@@ -51,11 +50,12 @@ struct GaCfg {
     static_assert(4 * 16 * DV * 4 + 2 * 4 * 16 * 4 <= OFF_Q, "merge scratch fits the rings");
 };
 
-template <int DQK, int DV>
-__global__ void __launch_bounds__(GA_THREADS, 2)
+// GA_STAGES = per-warp ring depth: 3 (two CTAs per SM) or 2 (three CTAs per SM)
+template <int DQK, int DV, int GA_STAGES>
+__global__ void __launch_bounds__(GA_THREADS, GA_STAGES == 2 ? 3 : 2)
 attn_gather_kernel(AttnArgs a)
 {
-    using C = GaCfg<DQK, DV>;
+    using C = GaCfg<DQK, DV, GA_STAGES>;
     extern __shared__ __align__(16) uint8_t smem[];
     bf16* Qs = reinterpret_cast<bf16*>(smem + C::OFF_Q);
     __shared__ int sh_flag;
@@ -273,17 +273,28 @@ attn_gather_kernel(AttnArgs a)
     }
 }
 
-template <int DQK, int DV>
-cudaError_t launch_ga(const AttnArgs& a, cudaStream_t s)
+template <int DQK, int DV, int ST>
+cudaError_t launch_ga_st(const AttnArgs& a, cudaStream_t s)
 {
-    using C = GaCfg<DQK, DV>;
-    cudaError_t e = cudaFuncSetAttribute(attn_gather_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    using C = GaCfg<DQK, DV, ST>;
+    cudaError_t e = cudaFuncSetAttribute(attn_gather_kernel<DQK, DV, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return e;
     }
     dim3 grid(a.rows, a.splits, (a.Hq + 15) / 16);
-    return launch_kernel(attn_gather_kernel<DQK, DV>, grid, dim3(GA_THREADS), (size_t)C::SMEM, s, a.pdl, a);
+    return launch_kernel(attn_gather_kernel<DQK, DV, ST>, grid, dim3(GA_THREADS), (size_t)C::SMEM, s, a.pdl, a);
+}
+
+// Many CTAs (a CTA per query row, prefill): occupancy hides the gather
+// latency best, so three CTAs per SM with two-stage rings. Few CTAs (split
+// decode rows): deeper three-stage rings, two CTAs per SM. Both measured.
+template <int DQK, int DV>
+cudaError_t launch_ga(const AttnArgs& a, cudaStream_t s)
+{
+    const int64_t ctas = (int64_t)a.rows * a.splits * ((a.Hq + 15) / 16);
+    if (ctas >= 4 * 148) return launch_ga_st<DQK, DV, 2>(a, s);
+    return launch_ga_st<DQK, DV, 3>(a, s);
 }
 
 }  // namespace

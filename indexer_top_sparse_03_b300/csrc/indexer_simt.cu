@@ -132,7 +132,10 @@ cudaError_t launch_indexer_simt(const IndexerArgs& a, cudaStream_t s)
 
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s)
 {
-    if (indexer_tc_supported(a)) return launch_indexer_tc(a, s);
+    if (indexer_tc_supported(a)) {
+        const cudaError_t e = launch_indexer_tc(a, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return launch_indexer_simt(a, s);
 }
 

@@ -44,6 +44,7 @@ namespace {
 
 constexpr int TC_BM = 128;                 // keys per tile (MMA M)
 constexpr int TC_BN = 256;                 // (query, head) pairs per tile (MMA N)
+constexpr int TC_ACC = 512 / TC_BN;        // TMEM accumulator buffers (all 512 columns)
 constexpr int TC_GROUP = 8;                // key tiles per work item
 constexpr int TC_EPI_WARPS = 16;                          // four per TMEM sub-partition
 constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
@@ -62,43 +63,53 @@ struct TcCfg {
     static constexpr int B_BUFS = (STAGES * A_BYTES + 2 * B_BYTES <= 160 * 1024) ? 2 : 1;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_W = OFF_B + B_BUFS * B_BYTES;
-    static constexpr int OFF_BAR = OFF_W + TC_BN * 4;
+    // staged score tiles (two) for the TMA store of tiles inside the causal window
+    static constexpr int C_BYTES = TQ * TC_BM * 4;
+    static constexpr int OFF_C = (OFF_W + TC_BN * 4 + 1023) / 1024 * 1024;
+    static constexpr bool TSTORE = (HI == 4 || HI == 8) && OFF_C + 2 * C_BYTES + 2048 <= 224 * 1024;
+    static constexpr int OFF_BAR = TSTORE ? OFF_C + 2 * C_BYTES : OFF_W + TC_BN * 4;
     // + barriers and alignment slack; never less than 116 KB, so that two CTAs
     // cannot share an SM (each holds all 512 TMEM columns)
-    static constexpr int SMEM_NEED = OFF_BAR + 256 + 1024;
+    static constexpr int SMEM_NEED = OFF_BAR + 8 * (2 * STAGES + 4 + 2 * TC_ACC) + 16 + 1024;
     static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
     static constexpr uint32_t IDESC = mma_idesc(ES == 2 ? 1u : 0u, TC_BM, TC_BN);
     static_assert(ROWB % KB == 0 && KB >= 32, "operand rows must be 32, 64 or a multiple of 128 bytes");
 };
 
 // Work items: query tile qi (TQ queries from t_begin + qi*TQ) x group g of
-// TC_GROUP key tiles. The walk below visits item blockIdx.x, then every
-// gridDim.x-th item after it, in (qi, g) order.
-struct ItemWalk {
-    int qi, g;
+// TC_GROUP key tiles (only tiles inside the causal window exist). The host
+// cuts the item sequence, in (qi, g) order, into one contiguous range per CTA
+// with about equal key-tile counts, and passes each CTA's first item; a CTA
+// then steps through its range item by item.
+constexpr int TC_MAX_CTAS = 256;
+
+struct TcSchedule {
+    int qi[TC_MAX_CTAS + 1];                // first item of CTA c is (qi[c], g[c]);
+    int g[TC_MAX_CTAS + 1];                 // entry gridDim.x is the end of the last range
 };
 
 template <int TQ>
-SA_DEVINL int item_groups(const IndexerArgs& a, int qi)
+__host__ __device__ inline int item_tiles_total(const IndexerArgs& a, int qi)
 {
     const int64_t t0 = (int64_t)a.t_begin + (int64_t)qi * TQ;
     const int64_t t_last = min64(t0 + TQ, a.T) - 1;
     const int64_t n_last = min64(a.N, max64(0, t_last + 1 + a.causal_offset));
-    const int64_t tiles = (n_last + TC_BM - 1) / TC_BM;
-    return (int)((tiles + TC_GROUP - 1) / TC_GROUP);
+    return (int)((n_last + TC_BM - 1) / TC_BM);
 }
 
+struct ItemWalk {
+    int qi, g, ng;                          // current item and its query tile's group count
+    int end_qi, end_g;
+    SA_DEVINL bool valid() const { return qi < end_qi || (qi == end_qi && g < end_g); }
+};
+
 template <int TQ>
-SA_DEVINL bool item_advance(const IndexerArgs& a, int nq, ItemWalk& w, int step)
+SA_DEVINL void item_next(const IndexerArgs& a, ItemWalk& w)
 {
-    w.g += step;
-    while (w.qi < nq) {
-        const int ng = item_groups<TQ>(a, w.qi);
-        if (w.g < ng) return true;
-        w.g -= ng;
-        ++w.qi;
-    }
-    return false;
+    if (++w.g < w.ng) return;
+    w.g = 0;
+    ++w.qi;
+    w.ng = (item_tiles_total<TQ>(a, w.qi) + TC_GROUP - 1) / TC_GROUP;
 }
 
 // Weighted ReLU head sum of one (key, query) score from its HI accumulator
@@ -128,8 +139,9 @@ SA_DEVINL float head_sum(const uint32_t* r, const float* w)
 }
 
 // Epilogue of one accumulator tile for one thread: TC_EPI_COLS columns of its
-// key (TC_EPI_COLS / HI queries), read from TMEM 32 columns at a time; the
-// accumulator is released as soon as the last columns are in registers. FULL
+// key (TC_EPI_COLS / HI queries). All of them are loaded from TMEM first and
+// the accumulator is released (one arrival per warp) before any arithmetic,
+// so the next MMA into this buffer overlaps the head sums and stores. FULL
 // tiles lie inside every query's causal window; the others test each
 // (query, key) pair: store iff t < T, j < N and j <= t + off.
 template <int HI, bool FULL, bool FP8>
@@ -138,18 +150,18 @@ SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int6
 {
     constexpr int QPC = 32 / HI;                       // queries per 32 columns
     constexpr int CH = TC_EPI_COLS / 32;
+    uint32_t r[CH][32];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) tmem_ld32(taddr + c * 32, r[c]);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
-        if (c == CH - 1) {
-            tc_fence_before();
-            mbar_arrive(empty_bar);
-        }
 #pragma unroll
         for (int qq = 0; qq < QPC; ++qq) {
-            float s = head_sum<HI>(&r[qq * HI], w + (c * QPC + qq) * HI);
+            float s = head_sum<HI>(&r[c][qq * HI], w + (c * QPC + qq) * HI);
             if (FP8) s *= ks;
             if (FULL) {
                 *p = s;
@@ -162,10 +174,47 @@ SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int6
     }
 }
 
+// Same as the FULL case of epi_tile, but the scores go to the staged tile in
+// shared memory (row = query, 128 keys per row; sc points at this thread's
+// first query and key), for one TMA store of the whole tile.
+template <int HI, bool FP8>
+SA_DEVINL void epi_tile_staged(uint32_t taddr, const float* w, float ks, float* sc, uint64_t* empty_bar)
+{
+    constexpr int QPC = 32 / HI;
+    constexpr int CH = TC_EPI_COLS / 32;
+    uint32_t r[CH][32];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) tmem_ld32(taddr + c * 32, r[c]);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+#pragma unroll
+        for (int qq = 0; qq < QPC; ++qq) {
+            float s = head_sum<HI>(&r[c][qq * HI], w + (c * QPC + qq) * HI);
+            if (FP8) s *= ks;
+            sc[(c * QPC + qq) * TC_BM] = s;
+        }
+    }
+}
+
+SA_DEVINL void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(m), "r"(x), "r"(y), "r"(smem_u32(src)) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+SA_DEVINL void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+SA_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+SA_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 template <int ES, int DI, int HI>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                  IndexerArgs a)
+                  const __grid_constant__ CUtensorMap tm_s, IndexerArgs a, int tstore,
+                  const __grid_constant__ TcSchedule sched)
 {
     using C = TcCfg<ES, DI, HI>;
     constexpr int TQ = C::TQ;
@@ -174,24 +223,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::OFF_B;
     float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
+    float* sC = reinterpret_cast<float*>(smem + C::OFF_C);     // [2][TQ][128] when C::TSTORE
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* a_full = bars;                       // [STAGES]
     uint64_t* a_empty = bars + C::STAGES;          // [STAGES]
     uint64_t* b_full = bars + 2 * C::STAGES;       // [2]
     uint64_t* b_empty = b_full + 2;                // [2]
-    uint64_t* acc_full = b_empty + 2;              // [2]
-    uint64_t* acc_empty = acc_full + 2;            // [2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* acc_full = b_empty + 2;              // [TC_ACC]
+    uint64_t* acc_empty = acc_full + TC_ACC;       // [TC_ACC]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + TC_ACC);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nq = (a.T - a.t_begin + TQ - 1) / TQ;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1);
-            mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS * 32);
-        }
+        for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
+        for (int i = 0; i < TC_ACC; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS); }
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_q);
@@ -202,15 +249,19 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    ItemWalk it{0, 0};
-    bool have = item_advance<TQ>(a, nq, it, blockIdx.x);
+    ItemWalk it;
+    it.qi = sched.qi[blockIdx.x];
+    it.g = sched.g[blockIdx.x];
+    it.ng = (item_tiles_total<TQ>(a, it.qi) + TC_GROUP - 1) / TC_GROUP;
+    it.end_qi = sched.qi[blockIdx.x + 1];
+    it.end_g = sched.g[blockIdx.x + 1];
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int s = 0, bb = 0;
             uint32_t aph = 0, bph = 0;
-            for (; have; have = item_advance<TQ>(a, nq, it, gridDim.x)) {
+            for (; it.valid(); item_next<TQ>(a, it)) {
                 const int t0 = a.t_begin + it.qi * TQ;
                 const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
                 const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
@@ -237,7 +288,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (lane == 0) {
             int s = 0, bb = 0, ab = 0;
             uint32_t aph = 0, bph = 0, acph = 0;
-            for (; have; have = item_advance<TQ>(a, nq, it, gridDim.x)) {
+            for (; it.valid(); item_next<TQ>(a, it)) {
                 const int t0 = a.t_begin + it.qi * TQ;
                 const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
                 const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
@@ -264,8 +315,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     tc_commit(&a_empty[s]);          // smem stage free once these MMAs finish
                     tc_commit(&acc_full[ab]);        // accumulator ready for the epilogue
                     if (++s == C::STAGES) { s = 0; aph ^= 1; }
-                    ab ^= 1;
-                    if (ab == 0) acph ^= 1;
+                    if (++ab == TC_ACC) { ab = 0; acph ^= 1; }
                 }
                 if (!ok) break;
                 tc_commit(&b_empty[bb]);
@@ -279,12 +329,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int half = (warp - 2) >> 2;               // which TC_EPI_COLS columns
         const int row = sub * 32 + lane;                // TMEM lane = key within the tile
         const bool fp8 = (ES == 1);
-        int ab = 0;
+        int ab = 0, tbuf = 0;
         uint32_t acph = 0;
         bool ok = true;
         // After a timed-out wait the loop keeps its shape (same named-barrier
         // count in every epilogue warp) but touches neither TMEM nor memory.
-        for (; have; have = item_advance<TQ>(a, nq, it, gridDim.x)) {
+        for (; it.valid(); item_next<TQ>(a, it)) {
             const int t0 = a.t_begin + it.qi * TQ;
             const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
             const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
@@ -310,24 +360,41 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int64_t j = (int64_t)kt * TC_BM + row;
                 const float ks = (fp8 && j < a.N) ? a.k_scale[j] : 1.0f;
                 const bool full = rows_full && (int64_t)kt * TC_BM + TC_BM <= n_first;
+                const bool staged = C::TSTORE && tstore && full;     // the same in every epilogue thread
                 if (ok) ok = mbar_wait(&acc_full[ab], acph, &g_tc_error);
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) continue;
-                tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * TC_EPI_COLS);
-                float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
-                const float* w_half = sW + tq_first * HI;
-                if (full)
-                    epi_tile<HI, true, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, 0, 0, 0, &acc_empty[ab]);
-                else
-                    epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a.T,
-                                                 a.causal_offset, &acc_empty[ab], a.N);
-                ab ^= 1;
-                if (ab == 0) acph ^= 1;
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * TC_EPI_COLS);
+                    const float* w_half = sW + tq_first * HI;
+                    if (staged) {
+                        float* sc = sC + tbuf * (TQ * TC_BM) + tq_first * TC_BM + row;
+                        epi_tile_staged<HI, ES == 1>(taddr, w_half, ks, sc, &acc_empty[ab]);
+                    } else {
+                        float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
+                        if (full)
+                            epi_tile<HI, true, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, 0, 0, 0, &acc_empty[ab]);
+                        else
+                            epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a.T,
+                                                         a.causal_offset, &acc_empty[ab], a.N);
+                    }
+                }
+                if (staged) {
+                    // make the staged tile visible to the TMA unit; the store
+                    // issued for the previous staged tile (other buffer) has
+                    // finished reading before anyone passes the barrier
+                    fence_proxy_async_smem();
+                    if (e == 0) bulk_wait_read_all();
+                    asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
+                    if (e == 0 && ok) tma_store_2d(&tm_s, sC + tbuf * (TQ * TC_BM), kt * TC_BM, t0 - a.t_begin);
+                    tbuf ^= 1;
+                }
+                if (++ab == TC_ACC) { ab = 0; acph ^= 1; }
             }
         }
     }
 
+    if (C::TSTORE && threadIdx.x == 64) bulk_wait_all();     // the last tile stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -343,27 +410,59 @@ template <int ES, int DI, int HI>
 cudaError_t launch_tc(const IndexerArgs& a, cudaStream_t s)
 {
     using C = TcCfg<ES, DI, HI>;
-    CUtensorMap tk, tq;
+    CUtensorMap tk, tq, ts;
     if (!make_tensor_map_2d(&tk, a.k_idx, ES, a.N, DI, DI, C::KB / ES, TC_BM) ||
         !make_tensor_map_2d(&tq, a.q_idx, ES, (int64_t)a.T * HI, DI, DI, C::KB / ES, TC_BN))
         return cudaErrorNotSupported;
-    // number of work items (host mirror of item_groups)
+    // scores tiles go out through TMA when the layout allows it (16-byte
+    // aligned rows); otherwise every score is stored by its thread
+    int tstore = 0;
+    if (C::TSTORE && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0 && a.ld_s % 4 == 0)
+        tstore = make_tensor_map_2d(&ts, a.scores, 4, a.T - a.t_begin, a.N, a.ld_s, TC_BM, C::TQ) ? 1 : 0;
+    if (!tstore) ts = tk;                     // unused
+    // items in (qi, g) order, cut into contiguous ranges of about equal tiles
     const int nq = (a.T - a.t_begin + C::TQ - 1) / C::TQ;
-    int64_t items = 0;
+    int64_t tiles = 0, items = 0;
     for (int qi = 0; qi < nq; ++qi) {
-        const int64_t t0 = (int64_t)a.t_begin + (int64_t)qi * C::TQ;
-        const int64_t t_last = min64(t0 + C::TQ, a.T) - 1;
-        const int64_t n_last = min64(a.N, max64(0, t_last + 1 + a.causal_offset));
-        items += ((n_last + TC_BM - 1) / TC_BM + TC_GROUP - 1) / TC_GROUP;
+        const int nt = item_tiles_total<C::TQ>(a, qi);
+        tiles += nt;
+        items += (nt + TC_GROUP - 1) / TC_GROUP;
     }
     if (items == 0) return cudaSuccess;
+    const int grid = (int)min64(min64(items, device_sm_count()), TC_MAX_CTAS);
+    TcSchedule sched;
+    int c = 0;
+    int64_t done = 0;
+    sched.qi[0] = 0;
+    sched.g[0] = 0;
+    for (int qi = 0; qi < nq && c + 1 < grid; ++qi) {
+        const int nt = item_tiles_total<C::TQ>(a, qi);
+        const int ng = (nt + TC_GROUP - 1) / TC_GROUP;
+        for (int g = 0; g < ng && c + 1 < grid; ++g) {
+            // start CTA c + 1 here once CTA c has its share of the tiles
+            if (done * grid >= tiles * (int64_t)(c + 1)) {
+                ++c;
+                sched.qi[c] = qi;
+                sched.g[c] = g;
+            }
+            done += min(TC_GROUP, nt - g * TC_GROUP);
+        }
+    }
+    for (int k = c + 1; k <= grid; ++k) {    // unused CTAs (and the end marker): past the last item
+        sched.qi[k] = nq;
+        sched.g[k] = 0;
+    }
     cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<ES, DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return e;
     }
-    const int grid = (int)min64(items, device_sm_count());
-    indexer_tc_kernel<ES, DI, HI><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, a);
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, indexer_tc_kernel<ES, DI, HI>) != cudaSuccess || fa.maxThreadsPerBlock < TC_THREADS) {
+        (void)cudaGetLastError();
+        return cudaErrorNotSupported;        // the caller falls back to the CUDA-core kernel
+    }
+    indexer_tc_kernel<ES, DI, HI><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, ts, a, tstore, sched);
     return cudaGetLastError();
 }
 
@@ -418,7 +517,8 @@ bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_
     const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                 : span == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
