@@ -192,6 +192,12 @@ def measured_peaks():
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
+def queue_ahead(torch, seconds: float):
+    """Hold the current stream on the device for about `seconds` (a bounded
+    spin), so that the launches enqueued meanwhile run back to back."""
+    torch.cuda._sleep(int(seconds * 2.0e9))
+
+
 def file_sha(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
@@ -328,6 +334,7 @@ def bench_prefill(sa, torch, dev, seed, name, iters):
                                out=out, idx_out=idx, stage_events=None if e is None else e[1:])
     step()
     torch.cuda.synchronize()
+    queue_ahead(torch, 0.02)
     for i in range(iters):
         step(ev[i])
     torch.cuda.synchronize()
@@ -393,9 +400,12 @@ def run_ours(args):
     value = aggregate_throughput(cfg.B, world, ms_step_max * 1e-3)
 
     # stage breakdown, measured separately (events between the stages break the
-    # programmatic launch chain, so these steps run a little slower)
+    # programmatic launch chain, so these steps run a little slower). The steps
+    # are queued behind a device-side delay, so that the host's launch time
+    # never shows up as idle time between two events.
     KS = min(K, 50)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KS)]
+    queue_ahead(torch, KS * 5e-4)
     for i in range(KS):
         ev[i][0].record()
         step(ev[i][1:])

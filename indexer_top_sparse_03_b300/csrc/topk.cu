@@ -7,18 +7,25 @@
 //   n <= 16384    the row's keys are staged in shared memory once, then an
 //                 MSB-first radix select (8-bit digits) finds the K-th key and
 //                 one ordered pass emits the kept positions.
-//   longer rows   a sample guides one streaming pass. A strided sample of
-//                 ~n/16 keys (8-key blocks, one 32-byte sector each) gives a
-//                 lower bound T_lo: the k'-th best sampled key, with k' the
-//                 sample's expected share of K plus a six-sigma margin, so
-//                 that almost surely at least K keys of the row reach T_lo
-//                 while only a few thousand do. The pass over the row keeps
-//                 the positions with key >= T_lo, in ascending order (block
-//                 prefix sums), as (key << 32 | ~position) composites; an exact
-//                 radix search over those composites then picks the K best and
-//                 they are emitted in order. If fewer than K or more than the
-//                 list holds reach T_lo, the row falls back to the radix select
-//                 over the whole row, so the result is exact in every case.
+//   longer rows   a sample guides one streaming pass:
+//     1. a strided sample of ~n/16 keys (blocks of 8 consecutive keys, one
+//        32-byte sector each) is counted into a 4096-bin histogram of the
+//        keys' top 12 bits, then the samples of the bin holding the k'-th
+//        best (k' = the sample's share of K plus a six-sigma margin) into a
+//        histogram of the next 12 bits; the resulting 24-bit prefix is a
+//        lower bound T_lo that at least K keys of the row reach almost
+//        surely, while only a few thousand do;
+//     2. one pass over the row keeps the positions with key >= T_lo, in
+//        ascending order (block prefix sums), as (key << 32 | ~position)
+//        composites;
+//     3. a 4096-bin histogram over equal slices of [T_lo, max candidate key]
+//        gives the slice of the K-th best; a radix search over the
+//        candidates of that slice alone finds the exact boundary (by key,
+//        then by lower position);
+//     4. the kept candidates are emitted in their (ascending) order.
+//   If fewer than K or more than the list holds reach T_lo, or the boundary
+//   bin is too crowded, the row falls back to the radix select over the whole
+//   row, so the result is exact in every case.
 // The output lists min(K, n) positions in ascending order, then -1 padding.
 #include "common.cuh"
 #include "kernels.h"
@@ -29,11 +36,13 @@ namespace {
 
 constexpr int TK_THREADS = 512;
 constexpr int STAGE_MAX = 16384;             // keys staged in shared memory (64 KB)
-constexpr int SAMPLE_MAX = 8192;             // sampled keys (32 KB)
-constexpr int CAND_CAP = 8192;               // candidate composites (64 KB)
+constexpr int SAMPLE_BLOCKS = 1024;          // sampled 8-key blocks at most
+constexpr int CAND_CAP = 5120;               // candidate composites (40 KB)
+constexpr int BIN_CAP = 1024;                // composites of the boundary bin (8 KB)
 constexpr int PER_THREAD = 16;               // consecutive positions per thread per pass step
-constexpr size_t TK_SMEM = (STAGE_MAX * 4 > SAMPLE_MAX * 4 + CAND_CAP * 8) ? STAGE_MAX * 4
-                                                                          : SAMPLE_MAX * 4 + CAND_CAP * 8;
+constexpr int SAMPLE_MAX = SAMPLE_BLOCKS * 8;     // sampled keys kept in shared memory (32 KB)
+constexpr size_t TK_SMEM_LONG = HBINS * 4 + SAMPLE_MAX * 4 + CAND_CAP * 8 + BIN_CAP * 8;
+constexpr size_t TK_SMEM = STAGE_MAX * 4 > TK_SMEM_LONG ? STAGE_MAX * 4 : TK_SMEM_LONG;
 
 SA_DEVINL int64_t topk_row_len(const TopkArgs& a, int r)
 {
@@ -41,71 +50,164 @@ SA_DEVINL int64_t topk_row_len(const TopkArgs& a, int r)
     return n < 0 ? 0 : (n > a.n_cap ? a.n_cap : n);
 }
 
+// 16 consecutive scores from position j0 as keys; positions >= n give 0
+// (below every score's key). Vector loads when the run is aligned and whole.
+SA_DEVINL void load16(const float* row, int64_t j0, int64_t n, bool aligned, uint32_t (&k)[PER_THREAD])
+{
+    if (aligned && j0 + PER_THREAD <= n) {
+        const float4* p = reinterpret_cast<const float4*>(row + j0);
+#pragma unroll
+        for (int i = 0; i < PER_THREAD / 4; ++i) {
+            const float4 v = __ldcs(p + i);
+            k[4 * i] = score_key(v.x); k[4 * i + 1] = score_key(v.y);
+            k[4 * i + 2] = score_key(v.z); k[4 * i + 3] = score_key(v.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < PER_THREAD; ++i) k[i] = j0 + i < n ? score_key(__ldcs(row + j0 + i)) : 0u;
+    }
+}
+
 // Sample-guided selection of a long row (n > STAGE_MAX). Returns false if the
-// sample's bound did not isolate between K and CAND_CAP candidates.
-__device__ bool sampled_select(const float* row, int64_t n, int K, int32_t* out, uint32_t* samp,
-                               unsigned long long* cand, RadixShared& sh)
+// sample's bound did not isolate between K and CAND_CAP candidates, or the
+// boundary bin holds more than BIN_CAP of them.
+__device__ bool sampled_select(const float* row, int64_t n, int K, int32_t* out, unsigned* hist,
+                               uint32_t* samp, unsigned long long* cand, unsigned long long* bcand,
+                               RadixShared& sh, BinSplit* split)
 {
     const int tid = threadIdx.x;
-    // 1. sample: blocks of 8 consecutive keys, one every S positions
-    const int64_t nblk_max = SAMPLE_MAX / 8;
-    const int64_t S = max64(16, ((n + nblk_max - 1) / nblk_max + 7) / 8 * 8);
+    const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    // 1. sample histogram: blocks of 8 consecutive keys, one every S positions
+    const int64_t S = max64(16, ((n + SAMPLE_BLOCKS - 1) / SAMPLE_BLOCKS + 7) / 8 * 8);
     const int nblk = (int)((n + S - 1) / S);
-    const int slots = nblk * 8;
-    for (int e = tid; e < slots; e += TK_THREADS) {
-        const int64_t j = (int64_t)(e >> 3) * S + (e & 7);
-        samp[e] = j < n ? score_key(__ldcg(row + j)) : 0u;      // 0 is below every score's key
+    for (int i = tid; i < HBINS; i += TK_THREADS) hist[i] = 0;
+    __syncthreads();
+    // warp-uniform trip count, so that the whole warp meets the match below
+    for (int b0 = tid & ~31; b0 < nblk; b0 += TK_THREADS) {
+        const int b = b0 + (tid & 31);
+        const int64_t j0 = (int64_t)b * S;
+        uint32_t k[8];
+        if (b >= nblk) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) k[i] = 0u;
+        } else if (aligned && j0 + 8 <= n) {
+            const float4 v0 = __ldcs(reinterpret_cast<const float4*>(row + j0));
+            const float4 v1 = __ldcs(reinterpret_cast<const float4*>(row + j0) + 1);
+            k[0] = score_key(v0.x); k[1] = score_key(v0.y); k[2] = score_key(v0.z); k[3] = score_key(v0.w);
+            k[4] = score_key(v1.x); k[5] = score_key(v1.y); k[6] = score_key(v1.z); k[7] = score_key(v1.w);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) k[i] = j0 + i < n ? score_key(__ldcs(row + j0 + i)) : 0u;
+        }
+        // samples crowd into few bins: one atomic per distinct bin per warp
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool valid = b < nblk && j0 + i < n;
+            if (b < nblk) samp[b * 8 + i] = valid ? k[i] : 0u;
+            const uint32_t bin = valid ? key_bin(k[i]) : (uint32_t)HBINS;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, bin);
+            if (bin < (uint32_t)HBINS && (threadIdx.x & 31) == __ffs(peers) - 1)
+                atomicAdd(&hist[bin], (unsigned)__popc(peers));
+        }
     }
     const int64_t tail = n - (int64_t)(nblk - 1) * S;
     const int m = (nblk - 1) * 8 + (int)min64(8, tail);          // valid samples
     const double share = (double)K * (double)m / (double)n;
     const double kq_d = ceil(share + 6.0 * sqrt(share) + 16.0);
-    if (kq_d >= (double)m) return false;
     __syncthreads();
-    uint32_t t_lo, t_mask;
-    radix_kth<uint32_t>(samp, (unsigned)slots, (unsigned)kq_d, sh, t_lo, t_mask);
+    if (kq_d >= (double)m) return false;
+    const BinSplit sb = find_bin(hist, (unsigned)kq_d, sh.warp_tot, split);
+    // refine inside that bin with the next 12 key bits, so that the bound sits
+    // just below the sample's k'-th best key rather than a whole bin lower
+    for (int i = tid; i < HBINS; i += TK_THREADS) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < nblk * 8; i += TK_THREADS) {
+        const uint32_t k = samp[i];
+        if (key_bin(k) == (uint32_t)sb.bin && k != 0u) atomicAdd(&hist[(k >> (HSHIFT - HBITS)) & (HBINS - 1)], 1u);
+    }
+    __syncthreads();
+    const BinSplit sb2 = find_bin(hist, (unsigned)kq_d - sb.above, sh.warp_tot, split);
+    const uint32_t lo = ((uint32_t)sb.bin << HSHIFT) | ((uint32_t)sb2.bin << (HSHIFT - HBITS));
 
-    // 2. one pass over the row: positions with key >= t_lo, in ascending order
-    const uint32_t lo = t_lo;
+    // 2. one pass over the row: positions with key >= lo, in ascending order;
+    //    the next step's loads are issued before this step's prefix sum
+    __shared__ uint32_t s_kmax;
+    if (tid == 0) s_kmax = lo;
     unsigned written = 0;
-    for (int64_t base = 0; base < n; base += (int64_t)TK_THREADS * PER_THREAD) {
+    uint32_t kmax = lo;
+    uint32_t kc[PER_THREAD], kn[PER_THREAD];
+    const int64_t step = (int64_t)TK_THREADS * PER_THREAD;
+    load16(row, (int64_t)tid * PER_THREAD, n, aligned, kn);
+    for (int64_t base = 0; base < n; base += step) {
+#pragma unroll
+        for (int i = 0; i < PER_THREAD; ++i) kc[i] = kn[i];
         const int64_t j0 = base + (int64_t)tid * PER_THREAD;
-        uint32_t keys[PER_THREAD];
+        if (base + step < n) load16(row, j0 + step, n, aligned, kn);
         unsigned c = 0;
 #pragma unroll
-        for (int u = 0; u < PER_THREAD; ++u) {
-            const int64_t j = j0 + u;
-            keys[u] = j < n ? score_key(__ldg(row + j)) : 0u;
-            c += (j < n && keys[u] >= lo) ? 1u : 0u;
-        }
+        for (int i = 0; i < PER_THREAD; ++i) c += (j0 + i < n && kc[i] >= lo) ? 1u : 0u;
         unsigned total;
         const unsigned incl = block_scan_incl(c, sh.warp_tot, &total);
         unsigned pos = written + incl - c;
 #pragma unroll
-        for (int u = 0; u < PER_THREAD; ++u) {
-            const int64_t j = j0 + u;
-            if (j < n && keys[u] >= lo) {
+        for (int i = 0; i < PER_THREAD; ++i) {
+            if (j0 + i < n && kc[i] >= lo) {
+                kmax = max(kmax, kc[i]);
                 if (pos < (unsigned)CAND_CAP)
-                    cand[pos] = ((unsigned long long)keys[u] << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+                    cand[pos] = ((unsigned long long)kc[i] << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)(j0 + i));
                 ++pos;
             }
         }
         written += total;
     }
-    if (written < (unsigned)K || written > (unsigned)CAND_CAP) return false;
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    if ((tid & 31) == 0) atomicMax(&s_kmax, kmax);
     __syncthreads();
+    if (written < (unsigned)K || written > (unsigned)CAND_CAP) return false;
 
-    // 3. the K best candidates (composites are distinct), emitted in order
+    // 3. the bin of the K-th best candidate, then the exact boundary inside it.
+    //    A candidate is taken relative to lo, rel = (key - lo) << 32 | ~pos;
+    //    the 4096 bins are equal slices of [lo, max key], 2^sh keys wide.
+    const uint32_t range = s_kmax - lo;
+    const int bsh = max(0, 32 - __clz((int)(range | 1u)) - HBITS);
+    auto rel = [&](unsigned long long c) -> unsigned long long {
+        return c - ((unsigned long long)lo << 32);
+    };
+    auto cbin = [&](unsigned long long c) -> uint32_t { return (uint32_t)(rel(c) >> (32 + bsh)); };
+    for (int i = tid; i < HBINS; i += TK_THREADS) hist[i] = 0;
+    __syncthreads();
+    for (unsigned i = tid; i < written; i += TK_THREADS) atomicAdd(&hist[cbin(cand[i])], 1u);
+    __syncthreads();
+    const BinSplit cb = find_bin(hist, (unsigned)K, sh.warp_tot, split);
+    if (cb.in_bin > (unsigned)BIN_CAP) return false;
+    // gather the boundary bin (any order: the search is order-free)
+    if (tid == 0) sh.cnt = 0;
+    __syncthreads();
+    for (unsigned i = tid; i < written; i += TK_THREADS) {
+        const unsigned long long c = cand[i];
+        if (cbin(c) == (uint32_t)cb.bin) bcand[atomicAdd(&sh.cnt, 1)] = rel(c);
+    }
+    __syncthreads();
+    // one bin's rel values agree above bit 32 + bsh: search from the digit
+    // holding bit 31 + bsh down (digits are 8 bits, ending at bit 0)
     unsigned long long prefix, mask;
-    radix_kth<unsigned long long>(cand, written, (unsigned)K, sh, prefix, mask);
+    radix_kth<unsigned long long>(bcand, cb.in_bin, (unsigned)K - cb.above, sh, prefix, mask,
+                                  (31 + bsh) / 8 * 8);
+
+    // 4. emit the kept candidates in their ascending order
     unsigned emitted = 0;
     for (unsigned i0 = 0; i0 < written; i0 += TK_THREADS) {
         const unsigned i = i0 + tid;
-        const bool keep = i < written && (cand[i] & mask) >= prefix;
+        bool keep = false;
+        unsigned long long c = 0;
+        if (i < written) {
+            c = cand[i];
+            const uint32_t bin = cbin(c);
+            keep = bin > (uint32_t)cb.bin || (bin == (uint32_t)cb.bin && (rel(c) & mask) >= prefix);
+        }
         unsigned total;
         const unsigned incl = block_scan_incl(keep ? 1u : 0u, sh.warp_tot, &total);
-        if (keep && emitted + incl - 1 < (unsigned)K)
-            out[emitted + incl - 1] = (int32_t)(0xFFFFFFFFu - (uint32_t)cand[i]);
+        if (keep && emitted + incl - 1 < (unsigned)K) out[emitted + incl - 1] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
         emitted += total;
     }
     return true;
@@ -115,6 +217,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 topk_rows_kernel(TopkArgs a)
 {
     __shared__ RadixShared sh;
+    __shared__ BinSplit split;
     extern __shared__ __align__(16) unsigned char tk_smem[];
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
@@ -134,9 +237,11 @@ topk_rows_kernel(TopkArgs a)
         radix_select_row([&](int64_t j) { return keys[j]; }, n, K, out, sh);
         return;
     }
-    uint32_t* samp = reinterpret_cast<uint32_t*>(tk_smem);
-    unsigned long long* cand = reinterpret_cast<unsigned long long*>(tk_smem + SAMPLE_MAX * 4);
-    if (!sampled_select(row, n, K, out, samp, cand, sh)) {
+    unsigned* hist = reinterpret_cast<unsigned*>(tk_smem);
+    uint32_t* samp = reinterpret_cast<uint32_t*>(tk_smem + HBINS * 4);
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(tk_smem + HBINS * 4 + SAMPLE_MAX * 4);
+    unsigned long long* bcand = cand + CAND_CAP;
+    if (!sampled_select(row, n, K, out, hist, samp, cand, bcand, sh, &split)) {
         __syncthreads();
         radix_select_row([&](int64_t j) { return score_key(__ldcg(row + j)); }, n, K, out, sh);
     }

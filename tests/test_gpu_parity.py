@@ -319,3 +319,17 @@ def test_decode_topk_all_scores_tied(sa):
     _, _, idx = _decode_with_indexer(sa, lens, 2048, lambda n: -np.ones(n), seed=42)
     for b, n in enumerate(lens):
         assert np.array_equal(idx[b], np.arange(2048))
+
+
+def test_topk_long_rows_crowded_boundary_bin(sa):
+    # long rows whose boundary bin holds thousands of tied keys (and rows whose
+    # candidate count overflows the list): both take the exact fallback path
+    rng = np.random.default_rng(17)
+    a = rng.random(20000).astype(np.float32) * 0.5
+    a[rng.choice(20000, 1500, replace=False)] = 5.0
+    rest = np.flatnonzero(a < 1.0)
+    a[rng.choice(rest, 3500, replace=False)] = 3.0
+    b = np.full(70000, 1.0, np.float32)
+    b[::7] = 2.0
+    c = rng.standard_normal(90000).astype(np.float32)          # the sampled path proper
+    _topk_case(sa, [a, b, c], 2048)
