@@ -2,6 +2,7 @@
 // the order of the launches. Every check runs on the host before anything is
 // enqueued; nothing here allocates device memory or synchronises.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "kernels.h"
@@ -31,11 +32,103 @@ int check_indexer_shape(int dtype, int Hi, int di)
 }
 
 // ---- prefill workspace layout --------------------------------------------
+// kept positions (if not returned) | score rows of one pass (also the scratch
+// rows of the fused path's fallback) | fused path: sampled keys, their
+// scales, sampled scores, thresholds, segment counts, segment pairs, failure
+// list
+//
+// Rows whose history is long enough take the fused path (indexer filter pass
+// + selection among the kept pairs); the plan fixes from which row on, and
+// the shape of every fused pass, on the host.
+constexpr int SAMPLE_LG = 4;                 // one sampled key per 16 positions
+
+struct FusePlan {
+    bool on;
+    int64_t t_fuse;          // first fused row
+    int64_t rows;            // rows per fused pass
+    int tq, lcap, cand_cap;
+    int64_t ns, ld_ssc, words;
+    int nseg_max;
+    size_t seg_words_max;    // max over passes of rows * nseg * cap_seg
+};
+
 struct PrefillLayout {
     int64_t rows_per_pass;   // query rows scored per indexer/Top-K pass
     int64_t ld_s;            // score row stride: L rounded up to a multiple of 4 (16-byte rows)
-    size_t idx_off, scores_off, total;
+    FusePlan fuse;
+    size_t idx_off, scores_off, ksamp_off, kscale_off, ssc_off, thr_off, cnt_off, seg_off, fail_off, total;
 };
+
+// pairs a row keeps at its threshold, generously: 16 x (K/16 + 6 sigma + 17)
+int64_t fused_expected_pairs(int K)
+{
+    const double share = K / 16.0;
+    return 16 * ((int64_t)ceil(share + 6.0 * sqrt(share) + 16.0) + 1);
+}
+
+// segments per row and pairs per segment of the fused pass over rows [t0, t1)
+void fused_pass_shape(int64_t t0, int64_t t1, int K, int& nseg, int& cap_seg)
+{
+    const double per_item = (double)sa::INDEXER_GROUP * 128.0 * (double)fused_expected_pairs(K) / (double)(t0 + 1);
+    cap_seg = (int)ceil(2.0 * per_item + 48.0);
+    nseg = (int)(((t1 + 127) / 128 + sa::INDEXER_GROUP - 1) / sa::INDEXER_GROUP);
+}
+
+// end of the fused pass that starts at t0: passes are aligned to end at L,
+// so that only the first one is partial
+int64_t fused_pass_end(const FusePlan& f, int64_t L, int64_t t0)
+{
+    const int64_t len = t0 == f.t_fuse ? (L - f.t_fuse - 1) % f.rows + 1 : f.rows;
+    return t0 + len < L ? t0 + len : L;
+}
+
+FusePlan fuse_plan(const sa_prefill_args& a, int64_t rows_per_pass)
+{
+    FusePlan f{};
+    sa::IndexerArgs ia{};
+    ia.dtype = a.idx_dtype; ia.Hi = a.Hi; ia.di = a.di;
+    f.lcap = sa::indexer_filter_lcap(ia);
+    if (f.lcap <= 64) return f;
+    f.tq = sa::indexer_query_tile(ia);
+    const int64_t E = fused_expected_pairs(a.K);
+    f.cand_cap = (int)((2 * E + 1023) / 1024 * 1024);
+    if (f.cand_cap < 8192) f.cand_cap = 8192;
+    if (f.cand_cap > 16384) return f;
+    // the first row whose per-item pairs fit the local lists twice over
+    int64_t n_req = (int64_t)ceil(2.0 * sa::INDEXER_GROUP * 128.0 * (double)E / (double)(f.lcap - 48));
+    if (n_req < 8 * (int64_t)a.K) n_req = 8 * (int64_t)a.K;
+    f.t_fuse = n_req - 1;
+    if (f.t_fuse >= a.L) return f;
+    f.ns = sa::sample_count(a.L - 1, SAMPLE_LG);
+    if (f.ns > 16384) return f;              // the threshold step's shared-memory row
+    f.ld_ssc = (f.ns + 3) / 4 * 4;
+    f.words = (a.L + 31) / 32;
+    // rows per fused pass: at most the score pass's rows (the fallback rescores
+    // into those rows), and few enough that the pair segments stay <= 256 MB
+    const int64_t t_req = f.t_fuse;
+    for (f.rows = rows_per_pass < 2048 ? rows_per_pass : 2048;; f.rows /= 2) {
+        // start on a pass boundary counted back from L when a whole pass fits
+        const int64_t whole = (a.L - t_req) / f.rows;
+        f.t_fuse = whole > 0 ? a.L - whole * f.rows : t_req;
+        f.nseg_max = 0;
+        f.seg_words_max = 0;
+        for (int64_t t0 = f.t_fuse; t0 < a.L; t0 = fused_pass_end(f, a.L, t0)) {
+            const int64_t t1 = fused_pass_end(f, a.L, t0);
+            int nseg, cap;
+            fused_pass_shape(t0, t1, a.K, nseg, cap);
+            if (cap > f.lcap) return f;
+            if (nseg > f.nseg_max) f.nseg_max = nseg;
+            const size_t w = (size_t)(t1 - t0) * nseg * cap;
+            if (w > f.seg_words_max) f.seg_words_max = w;
+        }
+        if (f.seg_words_max * 8 <= (size_t(256) << 20) || f.rows <= 128) break;
+    }
+    sa::FusedSelectArgs probe{};
+    probe.cand_cap = f.cand_cap; probe.words = f.words; probe.nseg = f.nseg_max;
+    if (sa::fused_select_smem(probe) > 200 * 1024) return f;
+    f.on = true;
+    return f;
+}
 
 PrefillLayout prefill_layout(const sa_prefill_args& a)
 {
@@ -46,11 +139,30 @@ PrefillLayout prefill_layout(const sa_prefill_args& a)
     int64_t rows = budget / (4 * (l.ld_s > 0 ? l.ld_s : 4));
     rows = rows < 1 ? 1 : (rows > L ? L : rows);
     l.rows_per_pass = rows;
+    l.fuse = fuse_plan(a, rows);
     size_t off = 0;
     l.idx_off = off;
     if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * (size_t)L * a.K);
     l.scores_off = off;
     off += align_up(sizeof(float) * (size_t)rows * (size_t)l.ld_s);
+    if (l.fuse.on) {
+        const FusePlan& f = l.fuse;
+        const size_t es = a.idx_dtype == SA_BF16 ? 2 : (a.idx_dtype == SA_FP8_E4M3 ? 1 : 4);
+        l.ksamp_off = off;
+        off += align_up((size_t)f.ns * a.di * es);
+        l.kscale_off = off;
+        off += align_up(sizeof(float) * (size_t)f.ns);
+        l.ssc_off = off;
+        off += align_up(sizeof(float) * (size_t)f.rows * (size_t)f.ld_ssc);
+        l.thr_off = off;
+        off += align_up(sizeof(uint32_t) * (size_t)f.rows);
+        l.cnt_off = off;
+        off += align_up(sizeof(unsigned) * (size_t)f.rows * (size_t)f.nseg_max);
+        l.seg_off = off;
+        off += align_up(sizeof(unsigned long long) * f.seg_words_max);
+        l.fail_off = off;
+        off += align_up(sizeof(unsigned) * (4 + (size_t)f.rows));
+    }
     l.total = off;
     return l;
 }
@@ -233,20 +345,68 @@ int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, 
     int32_t* idx = a.idx_out ? a.idx_out : reinterpret_cast<int32_t*>(wsb + lay.idx_off);
     float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
 
-    for (int64_t t0 = 0; t0 < a.L; t0 += lay.rows_per_pass) {
-        const int64_t t1 = (t0 + lay.rows_per_pass < a.L) ? t0 + lay.rows_per_pass : a.L;
+    const FusePlan& f = lay.fuse;
+    bool sampled = false;
+    for (int64_t t0 = 0; t0 < a.L;) {
+        const bool fused = f.on && t0 >= f.t_fuse;
+        int64_t t1 = fused ? fused_pass_end(f, a.L, t0) : t0 + lay.rows_per_pass;
+        if (f.on && !fused && t1 > f.t_fuse) t1 = f.t_fuse;
+        if (t1 > a.L) t1 = a.L;
         sa::IndexerArgs ia{};
         ia.q_idx = a.q_idx; ia.dtype = a.idx_dtype; ia.q_scale = a.q_scale; ia.w = a.w;
         ia.k_idx = a.k_idx; ia.k_scale = a.k_scale;
         ia.T = (int)t1; ia.N = (int)t1; ia.Hi = a.Hi; ia.di = a.di; ia.causal_offset = 0;
         ia.t_begin = (int)t0; ia.scores = scores; ia.ld_s = lay.ld_s;
-        cudaError_t e = sa::launch_indexer(ia, stream);
-        if (e != cudaSuccess) return SA_ERR_LAUNCH;
-        sa::TopkArgs ta{};
-        ta.scores = scores; ta.ld_s = lay.ld_s; ta.row_len = nullptr; ta.causal_first = t0;
-        ta.n_cap = a.L; ta.rows = (int)(t1 - t0); ta.K = a.K; ta.idx = idx + t0 * a.K; ta.ld_idx = a.K;
-        e = sa::launch_topk(ta, stream);
-        if (e != cudaSuccess) return SA_ERR_LAUNCH;
+        if (!fused) {
+            cudaError_t e = sa::launch_indexer(ia, stream);
+            if (e != cudaSuccess) return SA_ERR_LAUNCH;
+            sa::TopkArgs ta{};
+            ta.scores = scores; ta.ld_s = lay.ld_s; ta.row_len = nullptr; ta.causal_first = t0;
+            ta.n_cap = a.L; ta.rows = (int)(t1 - t0); ta.K = a.K; ta.idx = idx + t0 * a.K; ta.ld_idx = a.K;
+            e = sa::launch_topk(ta, stream);
+            if (e != cudaSuccess) return SA_ERR_LAUNCH;
+        } else {
+            void* ksamp = wsb + lay.ksamp_off;
+            float* kscale = reinterpret_cast<float*>(wsb + lay.kscale_off);
+            float* ssc = reinterpret_cast<float*>(wsb + lay.ssc_off);
+            unsigned* fail = reinterpret_cast<unsigned*>(wsb + lay.fail_off);
+            if (!sampled) {
+                const int es = a.idx_dtype == SA_BF16 ? 2 : (a.idx_dtype == SA_FP8_E4M3 ? 1 : 4);
+                if (sa::launch_sample_gather(a.k_idx, a.di * es, a.idx_dtype == SA_FP8_E4M3 ? a.k_scale : nullptr, f.ns,
+                                             SAMPLE_LG, ksamp, kscale, stream) != cudaSuccess)
+                    return SA_ERR_LAUNCH;
+                sampled = true;
+            }
+            // 1. scores against the sampled keys of every row's history
+            sa::IndexerArgs sia = ia;
+            sia.k_idx = ksamp; sia.k_scale = a.idx_dtype == SA_FP8_E4M3 ? kscale : nullptr;
+            sia.N = (int)f.ns; sia.sample_log2 = SAMPLE_LG; sia.scores = ssc; sia.ld_s = f.ld_ssc;
+            if (sa::launch_indexer(sia, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+            // 2. thresholds
+            sa::FusedSelectArgs fa{};
+            fa.t_begin = t0; fa.rows = (int)(t1 - t0); fa.N = t1; fa.K = a.K;
+            fa.tq = f.tq; fa.group = sa::INDEXER_GROUP; fa.sample_log2 = SAMPLE_LG; fa.ns = f.ns;
+            fa.thr = reinterpret_cast<uint32_t*>(wsb + lay.thr_off);
+            fa.seg_cnt = reinterpret_cast<unsigned*>(wsb + lay.cnt_off);
+            fa.seg_cand = reinterpret_cast<unsigned long long*>(wsb + lay.seg_off);
+            fused_pass_shape(t0, t1, a.K, fa.nseg, fa.cap_seg);
+            fa.cand_cap = f.cand_cap; fa.words = f.words;
+            fa.idx = idx + t0 * a.K; fa.ld_idx = a.K;
+            fa.fail_cnt = fail; fa.fail_list = reinterpret_cast<int*>(fail + 4);
+            fa.ia = ia; fa.scratch = scores; fa.ld_scratch = lay.ld_s;
+            if (sa::launch_sample_threshold(fa, ssc, f.ld_ssc, f.ns, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+            // 3. the filter pass: kept pairs per work item, no scores stored
+            sa::IndexerArgs fia = ia;
+            fia.scores = nullptr; fia.ld_s = 0;
+            fia.thr = fa.thr; fia.seg_cnt = reinterpret_cast<unsigned*>(wsb + lay.cnt_off);
+            fia.seg_cand = reinterpret_cast<unsigned long long*>(wsb + lay.seg_off);
+            fia.nseg = fa.nseg; fia.cap_seg = fa.cap_seg;
+            if (sa::launch_indexer_tc(fia, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+            // 4-5. exact selection, then the rows that need the fallback
+            if (sa::launch_zero(fail, 16, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+            if (sa::launch_fused_select(fa, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+        }
+        t0 = t1;
     }
     if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
     sa::AttnArgs at{};

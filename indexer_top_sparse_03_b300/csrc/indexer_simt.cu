@@ -28,7 +28,7 @@ indexer_simt_kernel(IndexerArgs a)
     const int t0 = a.t_begin + blockIdx.x * TQ;
     const int j0 = blockIdx.y * KEYS_PER_CTA;
     const int t_last = min(t0 + TQ, a.T) - 1;
-    const int64_t n_last = min64(a.N, max64(0, (int64_t)t_last + 1 + a.causal_offset));
+    const int64_t n_last = indexer_row_n(a, t_last);
     if (j0 >= n_last) return;               // the whole tile is beyond every row's history
 
     for (int i = threadIdx.x; i < TQ * HP * di; i += blockDim.x) {
@@ -95,7 +95,7 @@ indexer_simt_kernel(IndexerArgs a)
     for (int tq = 0; tq < TQ; ++tq) {
         const int t = t0 + tq;
         if (t >= a.T) break;
-        const int64_t n_t = min64(a.N, max64(0, (int64_t)t + 1 + a.causal_offset));
+        const int64_t n_t = indexer_row_n(a, t);
         if (j >= n_t) continue;
         float s = 0.0f;
 #pragma unroll
@@ -121,6 +121,7 @@ cudaError_t launch_hp(const IndexerArgs& a, cudaStream_t s)
 
 cudaError_t launch_indexer_simt(const IndexerArgs& a, cudaStream_t s)
 {
+    if (a.thr) return cudaErrorNotSupported;                 // filter mode is tensor-core only
     if (a.T - a.t_begin <= 0 || a.N <= 0) return cudaSuccess;
     if (a.Hi <= 1) return launch_hp<1>(a, s);
     if (a.Hi <= 2) return launch_hp<2>(a, s);

@@ -28,6 +28,12 @@
 //               taking a quarter of the 256 columns
 // Accumulators are double-buffered so that the epilogue of one key tile
 // overlaps the MMAs of the next. Every wait is bounded (see tc.cuh).
+//
+// Filter mode (the indexer fused with the first step of Top-K): instead of
+// storing every score, the epilogue keeps the (key, query) pairs whose score
+// reaches the query's threshold, collects them per query in shared memory
+// over a work item, and writes them out as that item's segment; nothing of
+// the score matrix reaches memory.
 #include <mutex>
 
 #include "common.cuh"
@@ -45,12 +51,12 @@ namespace {
 constexpr int TC_BM = 128;                 // keys per tile (MMA M)
 constexpr int TC_BN = 256;                 // (query, head) pairs per tile (MMA N)
 constexpr int TC_ACC = 512 / TC_BN;        // TMEM accumulator buffers (all 512 columns)
-constexpr int TC_GROUP = 8;                // key tiles per work item
+constexpr int TC_GROUP = INDEXER_GROUP;    // key tiles per work item
 constexpr int TC_EPI_WARPS = 16;                          // four per TMEM sub-partition
 constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 constexpr int TC_EPI_COLS = TC_BN * 4 / TC_EPI_WARPS;     // accumulator columns per epilogue thread
 
-template <int ES, int DI, int HI>
+template <int ES, int DI, int HI, bool FILTER = false>
 struct TcCfg {
     static constexpr int TQ = TC_BN / HI;                  // queries per tile
     static constexpr int ROWB = DI * ES;                   // bytes per operand row
@@ -63,15 +69,31 @@ struct TcCfg {
     static constexpr int B_BUFS = (STAGES * A_BYTES + 2 * B_BYTES <= 160 * 1024) ? 2 : 1;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_W = OFF_B + B_BUFS * B_BYTES;
-    // staged score tiles (two) for the TMA store of tiles inside the causal window
+    static constexpr int OFF_THR = OFF_W + TC_BN * 4;          // filter: TQ thresholds
+    static constexpr int OFF_CNT = OFF_THR + TQ * 4;           // filter: [TQ][4] local counts
+    // staged score tiles (two) for the TMA store of tiles inside the causal
+    // window; in filter mode the same space holds the local candidate lists
     static constexpr int C_BYTES = TQ * TC_BM * 4;
-    static constexpr int OFF_C = (OFF_W + TC_BN * 4 + 1023) / 1024 * 1024;
+    static constexpr int OFF_C = (OFF_CNT + TQ * 16 + 1023) / 1024 * 1024;
     static constexpr bool TSTORE = (HI == 4 || HI == 8) && OFF_C + 2 * C_BYTES + 2048 <= 224 * 1024;
-    static constexpr int OFF_BAR = TSTORE ? OFF_C + 2 * C_BYTES : OFF_W + TC_BN * 4;
-    // + barriers and alignment slack; never less than 116 KB, so that two CTAs
-    // cannot share an SM (each holds all 512 TMEM columns)
-    static constexpr int SMEM_NEED = OFF_BAR + 8 * (2 * STAGES + 4 + 2 * TC_ACC) + 16 + 1024;
+    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 4 + 2 * TC_ACC) + 16;
+    static constexpr int SMEM_MAX = 227 * 1024 - 1024;         // opt-in maximum less the alignment slack
+    // candidates per query and work item kept in shared memory (filter mode)
+    static constexpr int LCAP_FIT = (SMEM_MAX - OFF_C - BAR_BYTES) / (TQ * 8);
+    // a query's list is four sub-lists, one per TMEM sub-partition (each
+    // filled by the one warp that owns those 32 keys of the tile)
+    static constexpr int LCAP = (LCAP_FIT > 1024 ? 1024 : (LCAP_FIT < 4 ? 4 : LCAP_FIT)) / 4 * 4;
+    static constexpr int SUBCAP = LCAP / 4;
+    static constexpr bool FILTER_OK = LCAP_FIT >= 64;          // else filter mode is not offered
+    static constexpr int L_BYTES = FILTER && FILTER_OK ? TQ * LCAP * 8 : 0;
+    static constexpr int C_REGION = !FILTER && TSTORE ? 2 * C_BYTES : 0;
+    static constexpr int OFF_BAR = OFF_C + (C_REGION > L_BYTES ? C_REGION : L_BYTES);
+    // never less than 116 KB, so that two CTAs cannot share an SM (each holds
+    // all 512 TMEM columns)
+    static constexpr int SMEM_NEED = OFF_BAR + BAR_BYTES + 1024;
     static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(SUBCAP * 4 == LCAP, "four whole sub-lists per query");
     static constexpr uint32_t IDESC = mma_idesc(ES == 2 ? 1u : 0u, TC_BM, TC_BN);
     static_assert(ROWB % KB == 0 && KB >= 32, "operand rows must be 32, 64 or a multiple of 128 bytes");
 };
@@ -88,13 +110,14 @@ struct TcSchedule {
     int g[TC_MAX_CTAS + 1];                 // entry gridDim.x is the end of the last range
 };
 
+// key tiles of query tile qi: those below the last row's history end (row
+// lengths never decrease with t)
 template <int TQ>
 __host__ __device__ inline int item_tiles_total(const IndexerArgs& a, int qi)
 {
     const int64_t t0 = (int64_t)a.t_begin + (int64_t)qi * TQ;
     const int64_t t_last = min64(t0 + TQ, a.T) - 1;
-    const int64_t n_last = min64(a.N, max64(0, t_last + 1 + a.causal_offset));
-    return (int)((n_last + TC_BM - 1) / TC_BM);
+    return (int)((indexer_row_n(a, t_last) + TC_BM - 1) / TC_BM);
 }
 
 struct ItemWalk {
@@ -143,10 +166,10 @@ SA_DEVINL float head_sum(const uint32_t* r, const float* w)
 // the accumulator is released (one arrival per warp) before any arithmetic,
 // so the next MMA into this buffer overlaps the head sums and stores. FULL
 // tiles lie inside every query's causal window; the others test each
-// (query, key) pair: store iff t < T, j < N and j <= t + off.
+// (query, key) pair: store iff t < T and j < n_t.
 template <int HI, bool FULL, bool FP8>
 SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int64_t ld_s, int64_t j,
-                        int t_first, int T, int64_t off, uint64_t* empty_bar, int64_t N = 0)
+                        int t_first, const IndexerArgs& a, uint64_t* empty_bar)
 {
     constexpr int QPC = 32 / HI;                       // queries per 32 columns
     constexpr int CH = TC_EPI_COLS / 32;
@@ -167,7 +190,7 @@ SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int6
                 *p = s;
             } else {
                 const int t = t_first + c * QPC + qq;
-                if (t < T && j < N && j <= (int64_t)t + off) *p = s;
+                if (t < a.T && j < indexer_row_n(a, t)) *p = s;
             }
             p += ld_s;
         }
@@ -200,6 +223,55 @@ SA_DEVINL void epi_tile_staged(uint32_t taddr, const float* w, float ks, float* 
     }
 }
 
+// Filter-mode epilogue of one accumulator tile for one thread (one key j,
+// TC_EPI_COLS / HI queries): a pair is kept iff it is inside the query's
+// history and score_key(s) >= thr[q]. The warp ballots its 32 keys per query
+// and appends the kept ones to its own sub-list of the query (no other warp
+// writes there, so the count needs no atomic); counts keep growing past
+// subcap (the overflow is detected when the item is written out).
+template <int HI, bool FULL, bool FP8>
+SA_DEVINL void epi_filter(uint32_t taddr, const float* w, float ks, int64_t j, int t_first,
+                          const IndexerArgs& a, const uint32_t* thr, unsigned* cnt4,
+                          unsigned long long* lsub, int subcap, uint64_t* empty_bar)
+{
+    constexpr int QPC = 32 / HI;
+    constexpr int CH = TC_EPI_COLS / 32;
+    uint32_t r[CH][32];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) tmem_ld32(taddr + c * 32, r[c]);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) mbar_arrive(empty_bar);
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+#pragma unroll
+        for (int qq = 0; qq < QPC; ++qq) {
+            const int q = c * QPC + qq;
+            float s = head_sum<HI>(&r[c][qq * HI], w + q * HI);
+            if (FP8) s *= ks;
+            const uint32_t key = score_key(s);
+            bool pass = key >= thr[q];
+            if (!FULL) {
+                const int t = t_first + q;
+                pass = pass && t < a.T && j < indexer_row_n(a, t);
+            }
+            const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+            if (m) {                                   // warp-uniform
+                const unsigned base = cnt4[q * 4];     // this warp's count for query q
+                const unsigned slot = base + (unsigned)__popc(m & below);
+                if (pass && slot < (unsigned)subcap)
+                    lsub[(size_t)q * 4 * subcap + slot] =
+                        ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+                __syncwarp();
+                if (lane == 0) cnt4[q * 4] = base + (unsigned)__popc(m);
+            }
+        }
+    }
+}
+
 SA_DEVINL void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
@@ -210,13 +282,13 @@ SA_DEVINL void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.rea
 SA_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 SA_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-template <int ES, int DI, int HI>
+template <int ES, int DI, int HI, bool FILTER>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_s, IndexerArgs a, int tstore,
                   const __grid_constant__ TcSchedule sched)
 {
-    using C = TcCfg<ES, DI, HI>;
+    using C = TcCfg<ES, DI, HI, FILTER>;
     constexpr int TQ = C::TQ;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,6 +296,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* sB = smem + C::OFF_B;
     float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
     float* sC = reinterpret_cast<float*>(smem + C::OFF_C);     // [2][TQ][128] when C::TSTORE
+    uint32_t* sThr = reinterpret_cast<uint32_t*>(smem + C::OFF_THR);
+    unsigned* sCnt = reinterpret_cast<unsigned*>(smem + C::OFF_CNT);
+    unsigned long long* sL = reinterpret_cast<unsigned long long*>(smem + C::OFF_C);   // [TQ][LCAP], filter mode
+    constexpr bool filter = FILTER && C::FILTER_OK;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* a_full = bars;                       // [STAGES]
     uint64_t* a_empty = bars + C::STAGES;          // [STAGES]
@@ -263,7 +339,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             uint32_t aph = 0, bph = 0;
             for (; it.valid(); item_next<TQ>(a, it)) {
                 const int t0 = a.t_begin + it.qi * TQ;
-                const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
+                const int ntiles = item_tiles_total<TQ>(a, it.qi);
                 const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
                 if (!mbar_wait(&b_empty[bb], bph ^ 1, &g_tc_error)) break;
                 mbar_arrive_expect_tx(&b_full[bb], C::B_BYTES);
@@ -289,8 +365,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             int s = 0, bb = 0, ab = 0;
             uint32_t aph = 0, bph = 0, acph = 0;
             for (; it.valid(); item_next<TQ>(a, it)) {
-                const int t0 = a.t_begin + it.qi * TQ;
-                const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
+                const int ntiles = item_tiles_total<TQ>(a, it.qi);
                 const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
                 if (!mbar_wait(&b_full[bb], bph, &g_tc_error)) break;
                 tc_fence_after();
@@ -336,7 +411,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // count in every epilogue warp) but touches neither TMEM nor memory.
         for (; it.valid(); item_next<TQ>(a, it)) {
             const int t0 = a.t_begin + it.qi * TQ;
-            const int ntiles = (int)((min64(a.N, max64(0, (int64_t)min(t0 + TQ, a.T) + a.causal_offset)) + TC_BM - 1) / TC_BM);
+            const int ntiles = item_tiles_total<TQ>(a, it.qi);
             const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
             // head weights of this query tile (FP8: times the query-row scale)
             asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
@@ -349,34 +424,49 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 sW[i] = wv;
             }
+            if (filter && e < TQ) {
+                const int t = t0 + e;
+                sThr[e] = t < a.T ? a.thr[t - a.t_begin] : 0xFFFFFFFFu;
+                reinterpret_cast<uint4*>(sCnt)[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
             asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
 
             // tiles whose every key is visible to every query of the tile
             // skip the per-query causal mask
-            const int64_t n_first = min64(a.N, max64(0, (int64_t)t0 + 1 + a.causal_offset));
+            const int64_t n_first = indexer_row_n(a, t0);
             const bool rows_full = t0 + TQ <= a.T;
             const int tq_first = half * (TC_EPI_COLS / HI);
             for (int kt = k_begin; kt < k_end; ++kt) {
                 const int64_t j = (int64_t)kt * TC_BM + row;
                 const float ks = (fp8 && j < a.N) ? a.k_scale[j] : 1.0f;
                 const bool full = rows_full && (int64_t)kt * TC_BM + TC_BM <= n_first;
-                const bool staged = C::TSTORE && tstore && full;     // the same in every epilogue thread
+                const bool staged = !filter && C::TSTORE && tstore && full;   // the same in every epilogue thread
                 if (ok) ok = mbar_wait(&acc_full[ab], acph, &g_tc_error);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * TC_EPI_COLS);
                     const float* w_half = sW + tq_first * HI;
-                    if (staged) {
+                    if constexpr (filter) {
+                        // query q's sub-list `sub` starts at sL + (q * 4 + sub) * SUBCAP
+                        unsigned long long* lc = sL + ((size_t)tq_first * 4 + sub) * C::SUBCAP;
+                        unsigned* c4 = sCnt + tq_first * 4 + sub;
+                        if (full)
+                            epi_filter<HI, true, ES == 1>(taddr, w_half, ks, j, t0 + tq_first, a, sThr + tq_first,
+                                                          c4, lc, C::SUBCAP, &acc_empty[ab]);
+                        else
+                            epi_filter<HI, false, ES == 1>(taddr, w_half, ks, j, t0 + tq_first, a, sThr + tq_first,
+                                                           c4, lc, C::SUBCAP, &acc_empty[ab]);
+                    } else if (staged) {
                         float* sc = sC + tbuf * (TQ * TC_BM) + tq_first * TC_BM + row;
                         epi_tile_staged<HI, ES == 1>(taddr, w_half, ks, sc, &acc_empty[ab]);
                     } else {
                         float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
                         if (full)
-                            epi_tile<HI, true, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, 0, 0, 0, &acc_empty[ab]);
+                            epi_tile<HI, true, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, 0, a, &acc_empty[ab]);
                         else
-                            epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a.T,
-                                                         a.causal_offset, &acc_empty[ab], a.N);
+                            epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a,
+                                                         &acc_empty[ab]);
                     }
                 }
                 if (staged) {
@@ -390,6 +480,34 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     tbuf ^= 1;
                 }
                 if (++ab == TC_ACC) { ab = 0; acph ^= 1; }
+            }
+            if constexpr (filter) {
+                // the item's segment: query t0 + q of this item goes to
+                // segment it.g of its row; the count is the true one
+                asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
+                constexpr int TPQ = TC_EPI_WARPS * 32 / TQ;           // threads per query
+                const int q = e / TPQ, k0 = e % TPQ;
+                const int t = t0 + q;
+                if (ok && t < a.T) {
+                    const uint4 c4 = reinterpret_cast<const uint4*>(sCnt)[q];
+                    const unsigned cs[4] = {c4.x, c4.y, c4.z, c4.w};
+                    const unsigned cnt = c4.x + c4.y + c4.z + c4.w;
+                    const bool lost = c4.x > (unsigned)C::SUBCAP || c4.y > (unsigned)C::SUBCAP ||
+                                      c4.z > (unsigned)C::SUBCAP || c4.w > (unsigned)C::SUBCAP;
+                    const int64_t seg = (int64_t)(t - a.t_begin) * a.nseg + it.g;
+                    unsigned long long* dst = a.seg_cand + seg * a.cap_seg;
+                    if (!lost && cnt <= (unsigned)a.cap_seg) {
+                        unsigned off = 0;
+#pragma unroll
+                        for (int sb = 0; sb < 4; ++sb) {
+                            const unsigned long long* src = sL + ((size_t)q * 4 + sb) * C::SUBCAP;
+                            for (unsigned k = k0; k < cs[sb]; k += TPQ) dst[off + k] = src[k];
+                            off += cs[sb];
+                        }
+                    }
+                    // a sub-list that lost pairs makes the segment count as overflowed
+                    if (k0 == 0) a.seg_cnt[seg] = lost ? (unsigned)a.cap_seg + 1u : cnt;
+                }
             }
         }
     }
@@ -406,10 +524,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int ES, int DI, int HI>
-cudaError_t launch_tc(const IndexerArgs& a, cudaStream_t s)
+template <int ES, int DI, int HI, bool FILTER>
+cudaError_t launch_tc_mode(const IndexerArgs& a, cudaStream_t s)
 {
-    using C = TcCfg<ES, DI, HI>;
+    using C = TcCfg<ES, DI, HI, FILTER>;
     CUtensorMap tk, tq, ts;
     if (!make_tensor_map_2d(&tk, a.k_idx, ES, a.N, DI, DI, C::KB / ES, TC_BM) ||
         !make_tensor_map_2d(&tq, a.q_idx, ES, (int64_t)a.T * HI, DI, DI, C::KB / ES, TC_BN))
@@ -417,7 +535,7 @@ cudaError_t launch_tc(const IndexerArgs& a, cudaStream_t s)
     // scores tiles go out through TMA when the layout allows it (16-byte
     // aligned rows); otherwise every score is stored by its thread
     int tstore = 0;
-    if (C::TSTORE && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0 && a.ld_s % 4 == 0)
+    if (!FILTER && C::TSTORE && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0 && a.ld_s % 4 == 0)
         tstore = make_tensor_map_2d(&ts, a.scores, 4, a.T - a.t_begin, a.N, a.ld_s, TC_BM, C::TQ) ? 1 : 0;
     if (!tstore) ts = tk;                     // unused
     // items in (qi, g) order, cut into contiguous ranges of about equal tiles
@@ -452,18 +570,26 @@ cudaError_t launch_tc(const IndexerArgs& a, cudaStream_t s)
         sched.qi[k] = nq;
         sched.g[k] = 0;
     }
-    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<ES, DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<ES, DI, HI, FILTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return e;
     }
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, indexer_tc_kernel<ES, DI, HI>) != cudaSuccess || fa.maxThreadsPerBlock < TC_THREADS) {
+    if (cudaFuncGetAttributes(&fa, indexer_tc_kernel<ES, DI, HI, FILTER>) != cudaSuccess || fa.maxThreadsPerBlock < TC_THREADS) {
         (void)cudaGetLastError();
         return cudaErrorNotSupported;        // the caller falls back to the CUDA-core kernel
     }
-    indexer_tc_kernel<ES, DI, HI><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, ts, a, tstore, sched);
+    indexer_tc_kernel<ES, DI, HI, FILTER><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, ts, a, tstore, sched);
     return cudaGetLastError();
+}
+
+template <int ES, int DI, int HI>
+cudaError_t launch_tc(const IndexerArgs& a, cudaStream_t s)
+{
+    if (!a.thr) return launch_tc_mode<ES, DI, HI, false>(a, s);
+    if constexpr (TcCfg<ES, DI, HI, false>::FILTER_OK) return launch_tc_mode<ES, DI, HI, true>(a, s);
+    return cudaErrorNotSupported;
 }
 
 template <int ES, int DI>
@@ -533,6 +659,43 @@ int device_sm_count()
     return n;
 }
 
+template <int ES, int DI>
+int filter_lcap_hi(int Hi)
+{
+    switch (Hi) {
+    case 1: return TcCfg<ES, DI, 1>::FILTER_OK ? TcCfg<ES, DI, 1>::LCAP : 0;
+    case 2: return TcCfg<ES, DI, 2>::FILTER_OK ? TcCfg<ES, DI, 2>::LCAP : 0;
+    case 4: return TcCfg<ES, DI, 4>::FILTER_OK ? TcCfg<ES, DI, 4>::LCAP : 0;
+    case 8: return TcCfg<ES, DI, 8>::FILTER_OK ? TcCfg<ES, DI, 8>::LCAP : 0;
+    case 16: return TcCfg<ES, DI, 16>::FILTER_OK ? TcCfg<ES, DI, 16>::LCAP : 0;
+    case 32: return TcCfg<ES, DI, 32>::FILTER_OK ? TcCfg<ES, DI, 32>::LCAP : 0;
+    default: return 0;
+    }
+}
+
+int indexer_filter_lcap(const IndexerArgs& a)
+{
+    if (!indexer_tc_supported(a)) return 0;
+    if (a.dtype == SA_BF16) {
+        switch (a.di) {
+        case 16: return filter_lcap_hi<2, 16>(a.Hi);
+        case 32: return filter_lcap_hi<2, 32>(a.Hi);
+        case 64: return filter_lcap_hi<2, 64>(a.Hi);
+        case 128: return filter_lcap_hi<2, 128>(a.Hi);
+        default: return 0;
+        }
+    }
+    switch (a.di) {
+    case 32: return filter_lcap_hi<1, 32>(a.Hi);
+    case 64: return filter_lcap_hi<1, 64>(a.Hi);
+    case 128: return filter_lcap_hi<1, 128>(a.Hi);
+    case 256: return filter_lcap_hi<1, 256>(a.Hi);
+    default: return 0;
+    }
+}
+
+int indexer_query_tile(const IndexerArgs& a) { return a.Hi > 0 ? TC_BN / a.Hi : 0; }
+
 bool indexer_tc_supported(const IndexerArgs& a)
 {
     const bool hi_ok = a.Hi == 1 || a.Hi == 2 || a.Hi == 4 || a.Hi == 8 || a.Hi == 16 || a.Hi == 32;
@@ -545,6 +708,7 @@ bool indexer_tc_supported(const IndexerArgs& a)
 cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t s)
 {
     if (a.T - a.t_begin <= 0 || a.N <= 0) return cudaSuccess;
+    if (a.thr && indexer_filter_lcap(a) < a.cap_seg) return cudaErrorNotSupported;
     if (a.dtype == SA_BF16) {
         switch (a.di) {
         case 16: return launch_tc_hi<2, 16>(a, s);

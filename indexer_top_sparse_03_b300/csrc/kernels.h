@@ -53,11 +53,93 @@ struct IndexerArgs {
     int t_begin;            // first query row handled (rows t_begin .. T-1)
     float* scores;          // row t at scores + (t - t_begin) * ld_s
     int64_t ld_s;
+    // sampled keys: k_idx row i is the key sampled from stratum i (see
+    // sample_pos); then n_t = min(N, sample_count(t)) instead of the causal n_t
+    int sample_log2;        // 0: off
+    // filter mode (thr != null): no score is stored; a (query t, key j) pair
+    // with score_key(s) >= thr[t - t_begin] is appended, as the composite
+    // (score_key << 32 | ~j), to the segment of its work item: segment g of
+    // row r holds seg_cnt[r * nseg + g] entries (its true count, possibly above
+    // cap_seg, in which case only cap_seg were kept) at
+    // seg_cand + (r * nseg + g) * cap_seg
+    const uint32_t* thr;
+    unsigned* seg_cnt;
+    unsigned long long* seg_cand;
+    int nseg, cap_seg;
 };
+
+// ---- stratified key sample -------------------------------------------------
+// One key per stratum of 2^lg consecutive positions, at a pseudo-random offset
+// inside it: offset(i) = fmix32(i ^ SAMPLE_SEED) mod 2^lg, fmix32 being the
+// MurmurHash3 32-bit finaliser. A stratified sample keeps every key's
+// inclusion probability at 2^-lg whatever the structure of the positions.
+constexpr uint32_t SAMPLE_SEED = 0x9E3779B9u;
+__host__ __device__ inline uint32_t fmix32(uint32_t h)
+{
+    h ^= h >> 16;
+    h *= 0x85EBCA6Bu;
+    h ^= h >> 13;
+    h *= 0xC2B2AE35u;
+    h ^= h >> 16;
+    return h;
+}
+__host__ __device__ inline int64_t sample_pos(int64_t i, int lg)
+{
+    return (i << lg) + (int64_t)(fmix32((uint32_t)i ^ SAMPLE_SEED) & ((1u << lg) - 1u));
+}
+// number of sampled positions <= t
+__host__ __device__ inline int64_t sample_count(int64_t t, int lg)
+{
+    if (t < 0) return 0;
+    const int64_t full = (t + 1) >> lg;                      // strata wholly <= t
+    const int64_t part = (t + 1) & ((int64_t(1) << lg) - 1);  // positions of the next one <= t
+    return full + ((int64_t)(fmix32((uint32_t)full ^ SAMPLE_SEED) & ((1u << lg) - 1u)) < part ? 1 : 0);
+}
+// keys visible to query row t
+__host__ __device__ inline int64_t indexer_row_n(const IndexerArgs& a, int64_t t)
+{
+    const int64_t n = a.sample_log2 ? sample_count(t, a.sample_log2) : t + 1 + a.causal_offset;
+    return n < 0 ? 0 : (n > a.N ? a.N : n);
+}
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);        // picks one of:
 cudaError_t launch_indexer_simt(const IndexerArgs& a, cudaStream_t s);   // any dtype/shape, CUDA cores
 cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t s);     // bf16 / FP8, tensor cores
 bool indexer_tc_supported(const IndexerArgs& a);
+
+int indexer_filter_lcap(const IndexerArgs& a);   // pairs per query and work item in filter mode; 0: none
+int indexer_query_tile(const IndexerArgs& a);    // queries per tensor-core tile (256 / Hi)
+constexpr int INDEXER_GROUP = 8;                 // key tiles (of 128) per tensor-core work item
+
+// ---- steps 1+2 fused for long causal rows -----------------------------------
+struct FusedSelectArgs {
+    int64_t t_begin;        // rows t_begin .. t_begin + rows - 1, n_t = min(t + 1, N)
+    int rows;
+    int64_t N;
+    int K;
+    int tq, group;          // the filter pass's query-tile height and key tiles per item
+    int sample_log2;
+    int64_t ns;             // sampled keys
+    uint32_t* thr;          // [rows] threshold keys
+    const unsigned* seg_cnt;            // [rows][nseg]
+    const unsigned long long* seg_cand; // [rows][nseg][cap_seg]
+    int nseg, cap_seg;
+    int cand_cap;           // pairs of one row staged in shared memory
+    int64_t words;          // bitmap words of the longest row
+    int32_t* idx;           // row r at idx + r * ld_idx
+    int64_t ld_idx;
+    unsigned* fail_cnt;     // zeroed before the select
+    int* fail_list;         // [rows]
+    IndexerArgs ia;         // the full indexer problem (fallback rows are rescored from it)
+    float* scratch;         // fallback score rows: row r at scratch + r * ld_scratch
+    int64_t ld_scratch;
+};
+cudaError_t launch_sample_gather(const void* k_idx, int row_bytes, const float* k_scale, int64_t ns, int lg,
+                                 void* ksamp, float* ksamp_scale, cudaStream_t s);
+size_t fused_threshold_smem(int64_t max_samples);
+cudaError_t launch_sample_threshold(const FusedSelectArgs& a, const float* ssc, int64_t ld_ssc, int64_t max_samples,
+                                    cudaStream_t s);
+size_t fused_select_smem(const FusedSelectArgs& a);
+cudaError_t launch_fused_select(const FusedSelectArgs& a, cudaStream_t s);   // select + fallback
 
 // ---- step 2: Top-K over score rows -----------------------------------------
 struct TopkArgs {

@@ -131,8 +131,6 @@ __device__ bool sampled_select(const float* row, int64_t n, int K, int32_t* out,
 
     // 2. one pass over the row: positions with key >= lo, in ascending order;
     //    the next step's loads are issued before this step's prefix sum
-    __shared__ uint32_t s_kmax;
-    if (tid == 0) s_kmax = lo;
     unsigned written = 0;
     uint32_t kmax = lo;
     uint32_t kc[PER_THREAD], kn[PER_THREAD];
@@ -160,39 +158,12 @@ __device__ bool sampled_select(const float* row, int64_t n, int K, int32_t* out,
         }
         written += total;
     }
-    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-    if ((tid & 31) == 0) atomicMax(&s_kmax, kmax);
-    __syncthreads();
+    kmax = block_max_u32(kmax, sh.warp_tot);
     if (written < (unsigned)K || written > (unsigned)CAND_CAP) return false;
 
-    // 3. the bin of the K-th best candidate, then the exact boundary inside it.
-    //    A candidate is taken relative to lo, rel = (key - lo) << 32 | ~pos;
-    //    the 4096 bins are equal slices of [lo, max key], 2^sh keys wide.
-    const uint32_t range = s_kmax - lo;
-    const int bsh = max(0, 32 - __clz((int)(range | 1u)) - HBITS);
-    auto rel = [&](unsigned long long c) -> unsigned long long {
-        return c - ((unsigned long long)lo << 32);
-    };
-    auto cbin = [&](unsigned long long c) -> uint32_t { return (uint32_t)(rel(c) >> (32 + bsh)); };
-    for (int i = tid; i < HBINS; i += TK_THREADS) hist[i] = 0;
-    __syncthreads();
-    for (unsigned i = tid; i < written; i += TK_THREADS) atomicAdd(&hist[cbin(cand[i])], 1u);
-    __syncthreads();
-    const BinSplit cb = find_bin(hist, (unsigned)K, sh.warp_tot, split);
-    if (cb.in_bin > (unsigned)BIN_CAP) return false;
-    // gather the boundary bin (any order: the search is order-free)
-    if (tid == 0) sh.cnt = 0;
-    __syncthreads();
-    for (unsigned i = tid; i < written; i += TK_THREADS) {
-        const unsigned long long c = cand[i];
-        if (cbin(c) == (uint32_t)cb.bin) bcand[atomicAdd(&sh.cnt, 1)] = rel(c);
-    }
-    __syncthreads();
-    // one bin's rel values agree above bit 32 + bsh: search from the digit
-    // holding bit 31 + bsh down (digits are 8 bits, ending at bit 0)
-    unsigned long long prefix, mask;
-    radix_kth<unsigned long long>(bcand, cb.in_bin, (unsigned)K - cb.above, sh, prefix, mask,
-                                  (31 + bsh) / 8 * 8);
+    // 3. the exact boundary among the candidates
+    CandBoundary cb;
+    if (!cand_boundary(cand, written, lo, kmax, (unsigned)K, hist, bcand, BIN_CAP, sh, split, cb)) return false;
 
     // 4. emit the kept candidates in their ascending order
     unsigned emitted = 0;
@@ -202,8 +173,7 @@ __device__ bool sampled_select(const float* row, int64_t n, int K, int32_t* out,
         unsigned long long c = 0;
         if (i < written) {
             c = cand[i];
-            const uint32_t bin = cbin(c);
-            keep = bin > (uint32_t)cb.bin || (bin == (uint32_t)cb.bin && (rel(c) & mask) >= prefix);
+            keep = cand_keep(c, cb);
         }
         unsigned total;
         const unsigned incl = block_scan_incl(keep ? 1u : 0u, sh.warp_tot, &total);

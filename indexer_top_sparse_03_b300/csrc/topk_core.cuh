@@ -158,6 +158,82 @@ __device__ void radix_kth(const T* v, unsigned cnt, unsigned need, RadixShared& 
     mask_out = mask;
 }
 
+// ---------------------------------------------------------------------------
+// exact boundary inside a candidate list
+// ---------------------------------------------------------------------------
+// Candidates are composites c = (key << 32) | ~position (distinct, and the
+// larger composite is the better one: higher key, then lower position), all
+// with key >= lo. Relative to lo, rel(c) = c - (lo << 32); the 4096 bins are
+// equal slices of [lo, kmax], 2^bsh keys wide. A candidate is kept iff its
+// bin is above the boundary bin, or it is in that bin with
+// (rel & mask) >= prefix.
+struct CandBoundary {
+    uint32_t lo;
+    int bsh;
+    unsigned bin;
+    unsigned long long prefix, mask;
+};
+SA_DEVINL unsigned long long cand_rel(unsigned long long c, uint32_t lo)
+{
+    return c - ((unsigned long long)lo << 32);
+}
+SA_DEVINL uint32_t cand_bin(unsigned long long c, const CandBoundary& b)
+{
+    return (uint32_t)(cand_rel(c, b.lo) >> (32 + b.bsh));
+}
+SA_DEVINL bool cand_keep(unsigned long long c, const CandBoundary& b)
+{
+    const uint32_t bin = cand_bin(c, b);
+    return bin > b.bin || (bin == b.bin && (cand_rel(c, b.lo) & b.mask) >= b.prefix);
+}
+
+// Finds the boundary that keeps exactly K of the cnt >= K candidates cand[]
+// (shared or global memory). hist is 4096 words of shared scratch, bcand
+// room for bin_cap composites. Returns false (nothing decided) when the
+// boundary bin holds more than bin_cap candidates. Whole block.
+SA_DEVINL bool cand_boundary(const unsigned long long* cand, unsigned cnt, uint32_t lo, uint32_t kmax,
+                             unsigned K, unsigned* hist, unsigned long long* bcand, unsigned bin_cap,
+                             RadixShared& sh, BinSplit* split, CandBoundary& out)
+{
+    const int tid = threadIdx.x, nth = blockDim.x;
+    CandBoundary b;
+    b.lo = lo;
+    b.bsh = max(0, 32 - __clz((int)((kmax - lo) | 1u)) - HBITS);
+    for (int i = tid; i < HBINS; i += nth) hist[i] = 0;
+    __syncthreads();
+    for (unsigned i = tid; i < cnt; i += nth) atomicAdd(&hist[cand_bin(cand[i], b)], 1u);
+    __syncthreads();
+    const BinSplit cb = find_bin(hist, K, sh.warp_tot, split);
+    if (cb.in_bin > bin_cap) return false;
+    b.bin = (unsigned)cb.bin;
+    // gather the boundary bin (any order: the search is order-free)
+    if (tid == 0) sh.cnt = 0;
+    __syncthreads();
+    for (unsigned i = tid; i < cnt; i += nth) {
+        const unsigned long long c = cand[i];
+        if (cand_bin(c, b) == b.bin) bcand[atomicAdd(&sh.cnt, 1)] = cand_rel(c, lo);
+    }
+    __syncthreads();
+    // one bin's rel values agree above bit 32 + bsh: search from the digit
+    // holding bit 31 + bsh down (digits are 8 bits, ending at bit 0)
+    radix_kth<unsigned long long>(bcand, cb.in_bin, K - cb.above, sh, b.prefix, b.mask, (31 + b.bsh) / 8 * 8);
+    out = b;
+    return true;
+}
+
+// Block-wide maximum of one value per thread (shared scratch: 32 words).
+SA_DEVINL uint32_t block_max_u32(uint32_t v, unsigned* warp_tot)
+{
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane == 0) warp_tot[warp] = v;
+    __syncthreads();
+    uint32_t m = 0;
+    for (int w = 0; w < nw; ++w) m = max(m, (uint32_t)warp_tot[w]);
+    __syncthreads();
+    return m;
+}
+
 // Keeps the K best of the n keys given by key_at(j) (n > K) and writes their
 // positions in ascending order to out[0 .. K-1]. Whole block, blockDim.x a
 // multiple of 32.
