@@ -490,12 +490,37 @@ def main(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-prefill", type=int, default=0, metavar="L",
+                   help="for profiler captures only: run the FP8 128K-prefill shapes at length L\n"
+                        "(--steps calls, no timing, no JSON line) and exit")
     args = p.parse_args(argv)
+    if args.profile_prefill:
+        return profile_prefill(args)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
+
+
+def profile_prefill(args):
+    """A plain sequence of sparse_attn_prefill calls for ncu: the prefill_128k
+    shapes at length args.profile_prefill, args.steps calls."""
+    import torch
+
+    import indexer_top_sparse_03_b300 as sa
+    from workloads import get_config, make_prefill
+    sa.load_library()
+    cfg = get_config("prefill_128k", L=args.profile_prefill)
+    inp = make_prefill(cfg, seed=args.seed, device="cuda")
+    out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((cfg.L, cfg.K), dtype=torch.int32, device="cuda")
+    for _ in range(args.steps):
+        sa.sparse_attn_prefill(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], inp["w"], inp["gate"],
+                               cfg.K, 1 / math.sqrt(cfg.dqk), q_scale=inp["q_scale"], k_scale=inp["k_scale"],
+                               out=out, idx_out=idx)
+    torch.cuda.synchronize()
+    return 0
 
 
 if __name__ == "__main__":

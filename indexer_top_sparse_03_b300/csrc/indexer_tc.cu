@@ -71,11 +71,8 @@ struct TcCfg {
     static constexpr int OFF_W = OFF_B + B_BUFS * B_BYTES;
     static constexpr int OFF_THR = OFF_W + TC_BN * 4;          // filter: TQ thresholds
     static constexpr int OFF_CNT = OFF_THR + TQ * 4;           // filter: [TQ][4] local counts
-    // staged score tiles (two) for the TMA store of tiles inside the causal
-    // window; in filter mode the same space holds the local candidate lists
-    static constexpr int C_BYTES = TQ * TC_BM * 4;
+    // filter mode: the local candidate lists
     static constexpr int OFF_C = (OFF_CNT + TQ * 16 + 1023) / 1024 * 1024;
-    static constexpr bool TSTORE = (HI == 4 || HI == 8) && OFF_C + 2 * C_BYTES + 2048 <= 224 * 1024;
     static constexpr int BAR_BYTES = 8 * (2 * STAGES + 4 + 2 * TC_ACC) + 16;
     static constexpr int SMEM_MAX = 227 * 1024 - 1024;         // opt-in maximum less the alignment slack
     // candidates per query and work item kept in shared memory (filter mode)
@@ -86,8 +83,7 @@ struct TcCfg {
     static constexpr int SUBCAP = LCAP / 4;
     static constexpr bool FILTER_OK = LCAP_FIT >= 64;          // else filter mode is not offered
     static constexpr int L_BYTES = FILTER && FILTER_OK ? TQ * LCAP * 8 : 0;
-    static constexpr int C_REGION = !FILTER && TSTORE ? 2 * C_BYTES : 0;
-    static constexpr int OFF_BAR = OFF_C + (C_REGION > L_BYTES ? C_REGION : L_BYTES);
+    static constexpr int OFF_BAR = OFF_C + L_BYTES;
     // never less than 116 KB, so that two CTAs cannot share an SM (each holds
     // all 512 TMEM columns)
     static constexpr int SMEM_NEED = OFF_BAR + BAR_BYTES + 1024;
@@ -197,32 +193,6 @@ SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int6
     }
 }
 
-// Same as the FULL case of epi_tile, but the scores go to the staged tile in
-// shared memory (row = query, 128 keys per row; sc points at this thread's
-// first query and key), for one TMA store of the whole tile.
-template <int HI, bool FP8>
-SA_DEVINL void epi_tile_staged(uint32_t taddr, const float* w, float ks, float* sc, uint64_t* empty_bar)
-{
-    constexpr int QPC = 32 / HI;
-    constexpr int CH = TC_EPI_COLS / 32;
-    uint32_t r[CH][32];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) tmem_ld32(taddr + c * 32, r[c]);
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-#pragma unroll
-        for (int qq = 0; qq < QPC; ++qq) {
-            float s = head_sum<HI>(&r[c][qq * HI], w + (c * QPC + qq) * HI);
-            if (FP8) s *= ks;
-            sc[(c * QPC + qq) * TC_BM] = s;
-        }
-    }
-}
-
 // Filter-mode epilogue of one accumulator tile for one thread (one key j,
 // TC_EPI_COLS / HI queries): a pair is kept iff it is inside the query's
 // history and score_key(s) >= thr[q]. The warp ballots its 32 keys per query
@@ -272,21 +242,11 @@ SA_DEVINL void epi_filter(uint32_t taddr, const float* w, float ks, int64_t j, i
     }
 }
 
-SA_DEVINL void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-                 :: "l"(m), "r"(x), "r"(y), "r"(smem_u32(src)) : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-SA_DEVINL void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-SA_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-SA_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <int ES, int DI, int HI, bool FILTER>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_s, IndexerArgs a, int tstore,
-                  const __grid_constant__ TcSchedule sched)
+                  IndexerArgs a, const __grid_constant__ TcSchedule sched)
 {
     using C = TcCfg<ES, DI, HI, FILTER>;
     constexpr int TQ = C::TQ;
@@ -295,7 +255,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::OFF_B;
     float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
-    float* sC = reinterpret_cast<float*>(smem + C::OFF_C);     // [2][TQ][128] when C::TSTORE
     uint32_t* sThr = reinterpret_cast<uint32_t*>(smem + C::OFF_THR);
     unsigned* sCnt = reinterpret_cast<unsigned*>(smem + C::OFF_CNT);
     unsigned long long* sL = reinterpret_cast<unsigned long long*>(smem + C::OFF_C);   // [TQ][LCAP], filter mode
@@ -404,7 +363,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int half = (warp - 2) >> 2;               // which TC_EPI_COLS columns
         const int row = sub * 32 + lane;                // TMEM lane = key within the tile
         const bool fp8 = (ES == 1);
-        int ab = 0, tbuf = 0;
+        int ab = 0;
         uint32_t acph = 0;
         bool ok = true;
         // After a timed-out wait the loop keeps its shape (same named-barrier
@@ -436,11 +395,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int64_t n_first = indexer_row_n(a, t0);
             const bool rows_full = t0 + TQ <= a.T;
             const int tq_first = half * (TC_EPI_COLS / HI);
+            // FP8 key scales are loaded one tile ahead
+            auto key_scale = [&](int kt) -> float {
+                const int64_t jj = (int64_t)kt * TC_BM + row;
+                return (fp8 && jj < a.N) ? __ldg(a.k_scale + jj) : 1.0f;
+            };
+            float ks_next = key_scale(k_begin);
             for (int kt = k_begin; kt < k_end; ++kt) {
                 const int64_t j = (int64_t)kt * TC_BM + row;
-                const float ks = (fp8 && j < a.N) ? a.k_scale[j] : 1.0f;
+                const float ks = ks_next;
+                if (fp8 && kt + 1 < k_end) ks_next = key_scale(kt + 1);
                 const bool full = rows_full && (int64_t)kt * TC_BM + TC_BM <= n_first;
-                const bool staged = !filter && C::TSTORE && tstore && full;   // the same in every epilogue thread
                 if (ok) ok = mbar_wait(&acc_full[ab], acph, &g_tc_error);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
@@ -457,9 +422,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         else
                             epi_filter<HI, false, ES == 1>(taddr, w_half, ks, j, t0 + tq_first, a, sThr + tq_first,
                                                            c4, lc, C::SUBCAP, &acc_empty[ab]);
-                    } else if (staged) {
-                        float* sc = sC + tbuf * (TQ * TC_BM) + tq_first * TC_BM + row;
-                        epi_tile_staged<HI, ES == 1>(taddr, w_half, ks, sc, &acc_empty[ab]);
                     } else {
                         float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
                         if (full)
@@ -468,16 +430,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a,
                                                          &acc_empty[ab]);
                     }
-                }
-                if (staged) {
-                    // make the staged tile visible to the TMA unit; the store
-                    // issued for the previous staged tile (other buffer) has
-                    // finished reading before anyone passes the barrier
-                    fence_proxy_async_smem();
-                    if (e == 0) bulk_wait_read_all();
-                    asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
-                    if (e == 0 && ok) tma_store_2d(&tm_s, sC + tbuf * (TQ * TC_BM), kt * TC_BM, t0 - a.t_begin);
-                    tbuf ^= 1;
                 }
                 if (++ab == TC_ACC) { ab = 0; acph ^= 1; }
             }
@@ -512,7 +464,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
     }
 
-    if (C::TSTORE && threadIdx.x == 64) bulk_wait_all();     // the last tile stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -528,16 +479,10 @@ template <int ES, int DI, int HI, bool FILTER>
 cudaError_t launch_tc_mode(const IndexerArgs& a, cudaStream_t s)
 {
     using C = TcCfg<ES, DI, HI, FILTER>;
-    CUtensorMap tk, tq, ts;
+    CUtensorMap tk, tq;
     if (!make_tensor_map_2d(&tk, a.k_idx, ES, a.N, DI, DI, C::KB / ES, TC_BM) ||
         !make_tensor_map_2d(&tq, a.q_idx, ES, (int64_t)a.T * HI, DI, DI, C::KB / ES, TC_BN))
         return cudaErrorNotSupported;
-    // scores tiles go out through TMA when the layout allows it (16-byte
-    // aligned rows); otherwise every score is stored by its thread
-    int tstore = 0;
-    if (!FILTER && C::TSTORE && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0 && a.ld_s % 4 == 0)
-        tstore = make_tensor_map_2d(&ts, a.scores, 4, a.T - a.t_begin, a.N, a.ld_s, TC_BM, C::TQ) ? 1 : 0;
-    if (!tstore) ts = tk;                     // unused
     // items in (qi, g) order, cut into contiguous ranges of about equal tiles
     const int nq = (a.T - a.t_begin + C::TQ - 1) / C::TQ;
     int64_t tiles = 0, items = 0;
@@ -580,7 +525,7 @@ cudaError_t launch_tc_mode(const IndexerArgs& a, cudaStream_t s)
         (void)cudaGetLastError();
         return cudaErrorNotSupported;        // the caller falls back to the CUDA-core kernel
     }
-    indexer_tc_kernel<ES, DI, HI, FILTER><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, ts, a, tstore, sched);
+    indexer_tc_kernel<ES, DI, HI, FILTER><<<grid, TC_THREADS, C::SMEM, s>>>(tk, tq, a, sched);
     return cudaGetLastError();
 }
 
@@ -631,7 +576,7 @@ static EncodeTiledFn encode_fn()
 }
 
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, int64_t cols,
-                        int64_t row_stride_elems, int box_cols, int box_rows)
+                        int64_t row_stride_elems, int box_cols, int box_rows, bool swizzle)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -640,7 +585,8 @@ bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const int span = box_cols * elem_bytes;
-    const CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+    const CUtensorMapSwizzle sw = !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                : span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                 : span == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
     const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32

@@ -13,8 +13,9 @@ namespace sa {
 // 2D TMA descriptor of a row-major matrix of 1-, 2- or 4-byte elements
 // (bytes, bf16, fp32); swizzle = the box's row bytes when 32, 64 or 128,
 // else none.
+// swizzle: the box's inner span picks 128/64/32-byte swizzling (else none)
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, int64_t cols,
-                        int64_t row_stride_elems, int box_cols, int box_rows);
+                        int64_t row_stride_elems, int box_cols, int box_rows, bool swizzle = true);
 int device_sm_count();
 
 // Kernel launch, optionally as a programmatic dependent of the previous work
