@@ -26,6 +26,8 @@ Layer steps and where the pages state them:
               (token, head) ("Sparse Attention and Hybrid Attention
               Architecture Design", section 4, output gating; section 3.3 of
               the first page returns gate * attn_out).
+  attend_backward -- the gradients of the gated attention over a fixed
+              index set (the training path), by the chain rule.
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -74,6 +76,9 @@ def _load():
         lib.oracle_attend.argtypes = [P, I, I, I, I, P, I64, P, I64, I64, P, P, P, I, D, P,
                                       P, P, I]
         lib.oracle_attend.restype = I
+        lib.oracle_attend_backward.argtypes = [P, I, I, I, I, P, I64, P, I64, I64, P, P, P, I, D, P, P,
+                                               P, P, P, P, I]
+        lib.oracle_attend_backward.restype = I
         _lib = lib
     return _lib
 
@@ -190,6 +195,37 @@ def attend(q, k_cache, v_cache, ld_k, ld_v, dv, gate, qrow, key_start, idx, scal
     if rc != 0:
         raise RuntimeError(f"oracle_attend failed ({rc})")
     return (out, pre) if want_pre else out
+
+
+def attend_backward(q, k, v, ld_k, ld_v, dv, gate, qrow, key_start, idx, scale, dout, n_keys,
+                    nthreads: int = 0):
+    """Gradients of sum(dout * out) for out = attend(...) over the fixed index
+    set idx (the training path: section 3.1 of the first page, the selected set
+    is fixed; section 3.3, the gate). dout [R, Hq, dv] in the storage type of
+    q. Returns float64 dq [R, Hq, dqk], dk [n_keys, dqk], dv [n_keys, dv] (the
+    key and value rows' totals over every task) and dgate [R, Hq] (with
+    respect to the gate logits)."""
+    qa, qd = _raw(q)
+    ka, kd = _raw(k)
+    va, vd = _raw(v)
+    da, dd = _raw(dout)
+    if not (qd == kd == vd == dd):
+        raise TypeError("q, k, v and dout must share a storage type")
+    _, Hq, dqk = q.shape
+    qrow, key_start = _i64(qrow), _i64(key_start)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    R, K = idx.shape
+    dq = np.empty((R, Hq, dqk), dtype=np.float64)
+    dk = np.zeros((n_keys, dqk), dtype=np.float64)
+    dvv = np.zeros((n_keys, dv), dtype=np.float64)
+    dgate = np.empty((R, Hq), dtype=np.float64)
+    ga = _f32(gate)
+    rc = _load().oracle_attend_backward(_ptr(qa), qd, Hq, dqk, dv, _ptr(ka), ld_k, _ptr(va), ld_v, R,
+                                        _ptr(qrow), _ptr(key_start), _ptr(idx), K, float(scale), _ptr(ga),
+                                        _ptr(da), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dgate), nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_attend_backward failed ({rc})")
+    return dq, dk, dvv, dgate
 
 
 # ---------------------------------------------------------------------------

@@ -320,3 +320,138 @@ int oracle_attend(const void* q, int dtype, int Hq, int dqk, int dv,
     run_rows(attend_row, &c, ntasks, nthreads);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* gradients of the gated attention over a fixed index set             */
+/* ------------------------------------------------------------------ */
+/*
+ * The training path of the layer ("Hybrid Attention Architectures...",
+ * section 3.1: the selected set is fixed once the indexer has chosen it, and
+ * attention over it is ordinary softmax attention; the gate of section 3.3
+ * scales its output). For task r (query row t = qrow[r], keys key_start[r] +
+ * idx[r, i], idx < 0 skipped), with l_i = scale * q_h . k_i, p = softmax(l),
+ * o_h = sum_i p_i v_i, g_h = 1 / (1 + exp(-x_h)) and out_h = g_h o_h, the
+ * derivatives of sum(dout * out) are, by the chain rule:
+ *     dx_h  = g_h (1 - g_h) (dout_h . o_h)
+ *     do_h  = g_h dout_h
+ *     dp_i  = do_h . v_i,   D_h = sum_i p_i dp_i
+ *     dl_i  = p_i (dp_i - D_h)
+ *     dq_h  = scale sum_i dl_i k_i
+ *     dk_i += scale sum_h dl_i q_h,   dv_i += sum_h p_i do_h
+ * dq [ntasks, Hq, dqk] and dgate [ntasks, Hq] are per task; dk [nk, dqk] and
+ * dv [nk, dv] collect every task's share (rows of the key and value arrays,
+ * which the caller zeroes). dq and dgate run row-parallel; the shared dk and
+ * dv are accumulated afterwards, one task after the other, in task order.
+ */
+typedef struct {
+    const void* q; int dtype; int Hq, dqk, dv;
+    const void* kc; int64_t ld_k; const void* vc; int64_t ld_v;
+    const int64_t *qrow, *key_start; const int32_t* idx; int K;
+    double scale; const float* gate; const void* dout;
+    double *dq, *dk, *dvo, *dgate;
+} backward_ctx;
+
+/* p (softmax weights) and dl (logit gradients) of one (task, head); o is
+ * the pre-gate output; returns dout . o */
+static double backward_head(const backward_ctx* c, int64_t r, int h, double* q, double* p, double* dl,
+                            double* o, double* dout, double* g_out)
+{
+    const int64_t t = c->qrow[r];
+    const int32_t* sel = c->idx + r * (int64_t)c->K;
+    for (int d = 0; d < c->dqk; ++d) q[d] = load_elem(c->q, c->dtype, (t * c->Hq + h) * (int64_t)c->dqk + d);
+    for (int e = 0; e < c->dv; ++e) dout[e] = load_elem(c->dout, c->dtype, (r * c->Hq + h) * (int64_t)c->dv + e);
+    double m = -INFINITY;
+    for (int i = 0; i < c->K; ++i) {
+        if (sel[i] < 0) continue;
+        const int64_t kr = c->key_start[r] + sel[i];
+        double dot = 0.0;
+        for (int d = 0; d < c->dqk; ++d) dot += q[d] * load_elem(c->kc, c->dtype, kr * c->ld_k + d);
+        p[i] = c->scale * dot;
+        if (p[i] > m) m = p[i];
+    }
+    double denom = 0.0;
+    for (int i = 0; i < c->K; ++i) {
+        if (sel[i] < 0) continue;
+        p[i] = exp(p[i] - m);
+        denom += p[i];
+    }
+    for (int e = 0; e < c->dv; ++e) o[e] = 0.0;
+    for (int i = 0; i < c->K; ++i) {
+        if (sel[i] < 0) continue;
+        p[i] /= denom;
+        const int64_t kr = c->key_start[r] + sel[i];
+        for (int e = 0; e < c->dv; ++e) o[e] += p[i] * load_elem(c->vc, c->dtype, kr * c->ld_v + e);
+    }
+    const double g = 1.0 / (1.0 + exp(-(double)c->gate[t * c->Hq + h]));
+    double dout_o = 0.0;
+    for (int e = 0; e < c->dv; ++e) dout_o += dout[e] * o[e];
+    /* D = do . o with do = g * dout */
+    const double D = g * dout_o;
+    for (int i = 0; i < c->K; ++i) {
+        if (sel[i] < 0) continue;
+        const int64_t kr = c->key_start[r] + sel[i];
+        double dp = 0.0;
+        for (int e = 0; e < c->dv; ++e) dp += g * dout[e] * load_elem(c->vc, c->dtype, kr * c->ld_v + e);
+        dl[i] = p[i] * (dp - D);
+    }
+    *g_out = g;
+    return dout_o;
+}
+
+static void backward_row(void* pc, int64_t r)
+{
+    backward_ctx* c = (backward_ctx*)pc;
+    const int32_t* sel = c->idx + r * (int64_t)c->K;
+    double* q = (double*)malloc(sizeof(double) * (size_t)c->dqk);
+    double* o = (double*)malloc(sizeof(double) * (size_t)c->dv);
+    double* dout = (double*)malloc(sizeof(double) * (size_t)c->dv);
+    double* p = (double*)malloc(sizeof(double) * (size_t)c->K);
+    double* dl = (double*)malloc(sizeof(double) * (size_t)c->K);
+    for (int h = 0; h < c->Hq; ++h) {
+        double g;
+        const double dout_o = backward_head(c, r, h, q, p, dl, o, dout, &g);
+        c->dgate[r * c->Hq + h] = g * (1.0 - g) * dout_o;
+        double* dq = c->dq + (r * c->Hq + h) * (int64_t)c->dqk;
+        for (int d = 0; d < c->dqk; ++d) dq[d] = 0.0;
+        for (int i = 0; i < c->K; ++i) {
+            if (sel[i] < 0) continue;
+            const int64_t kr = c->key_start[r] + sel[i];
+            for (int d = 0; d < c->dqk; ++d) dq[d] += c->scale * dl[i] * load_elem(c->kc, c->dtype, kr * c->ld_k + d);
+        }
+    }
+    free(q); free(o); free(dout); free(p); free(dl);
+}
+
+int oracle_attend_backward(const void* q, int dtype, int Hq, int dqk, int dv,
+                           const void* k_cache, int64_t ld_k, const void* v_cache, int64_t ld_v,
+                           int64_t ntasks, const int64_t* qrow, const int64_t* key_start,
+                           const int32_t* idx, int K, double scale, const float* gate, const void* dout,
+                           double* dq, double* dk, double* dvo, double* dgate, int nthreads)
+{
+    if (dtype != OR_F32 && dtype != OR_BF16) return -1;
+    if (Hq <= 0 || dqk <= 0 || dv <= 0 || K <= 0) return -1;
+    backward_ctx c = { q, dtype, Hq, dqk, dv, k_cache, ld_k, v_cache, ld_v, qrow, key_start, idx, K,
+                       scale, gate, dout, dq, dk, dvo, dgate };
+    run_rows(backward_row, &c, ntasks, nthreads);
+    /* the shared key and value rows, one task after the other */
+    double* qv = (double*)malloc(sizeof(double) * (size_t)dqk);
+    double* o = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* dov = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* p = (double*)malloc(sizeof(double) * (size_t)K);
+    double* dl = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t r = 0; r < ntasks; ++r) {
+        const int32_t* sel = idx + r * (int64_t)K;
+        for (int h = 0; h < Hq; ++h) {
+            double g;
+            (void)backward_head(&c, r, h, qv, p, dl, o, dov, &g);
+            for (int i = 0; i < K; ++i) {
+                if (sel[i] < 0) continue;
+                const int64_t kr = key_start[r] + sel[i];
+                for (int d = 0; d < dqk; ++d) dk[kr * dqk + d] += scale * dl[i] * qv[d];
+                for (int e = 0; e < dv; ++e) dvo[kr * dv + e] += p[i] * g * dov[e];
+            }
+        }
+    }
+    free(qv); free(o); free(dov); free(p); free(dl);
+    return 0;
+}

@@ -288,6 +288,85 @@ def test_attend_latent_row_values_alias_keys():
 
 
 # ---------------------------------------------------------------------------
+# gradients over a fixed index set
+# ---------------------------------------------------------------------------
+
+def _bwd_case(seed, L=11, Hq=3, d=8, K=6):
+    q, k, v = _rand((L, Hq, d), seed), _rand((L, d), seed + 1), _rand((L, d), seed + 2)
+    gate, dout = _rand((L, Hq), seed + 3), _rand((L, Hq, d), seed + 4)
+    rng = np.random.default_rng(seed)
+    idx = np.full((L, K), -1, dtype=np.int32)
+    for t in range(L):                       # a causal selection, some rows short
+        m = min(K, t + 1)
+        idx[t, :m] = np.sort(rng.choice(t + 1, size=m, replace=False))
+    return q, k, v, gate, dout, idx
+
+
+def test_backward_matches_float64_autograd():
+    L, Hq, d, K, scale = 11, 3, 8, 6, 0.3
+    q, k, v, gate, dout, idx = _bwd_case(40, L, Hq, d, K)
+    dq, dk, dv, dg = oracle.attend_backward(q, k, v, d, d, d, gate, np.arange(L), np.zeros(L), idx, scale,
+                                            dout, n_keys=L)
+    # the same forward in torch float64; autograd derives the gradients
+    qt, kt, vt, gt = (x.double().requires_grad_() for x in (q, k, v, gate))
+    outs = []
+    for t in range(L):
+        sel = torch.as_tensor(idx[t][idx[t] >= 0], dtype=torch.long)
+        p = torch.softmax(scale * qt[t] @ kt[sel].T, dim=-1)
+        outs.append(torch.sigmoid(gt[t]).unsqueeze(-1) * (p @ vt[sel]))
+    (torch.stack(outs) * dout.double()).sum().backward()
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dg, gt.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def test_backward_matches_central_differences_of_the_forward():
+    L, Hq, d, K, scale = 7, 2, 4, 4, 0.7
+    q, k, v, gate, dout, idx = _bwd_case(50, L, Hq, d, K)
+    dq, dk, dv, dg = oracle.attend_backward(q, k, v, d, d, d, gate, np.arange(L), np.zeros(L), idx, scale,
+                                            dout, n_keys=L)
+    dd = dout.double().numpy()
+
+    def loss(qq, kk, vv, gg):
+        out = oracle.attend(qq, kk, vv, d, d, d, gg, np.arange(L), np.zeros(L), idx, scale)
+        return float((out * dd).sum())
+
+    def secant(t, pos, analytic, which):
+        lo, hi = t.clone(), t.clone()
+        x = float(t[pos])
+        lo[pos], hi[pos] = x - 1e-3, x + 1e-3      # stored fp32: the secant uses the stored values
+        args_lo = [q, k, v, gate]
+        args_hi = [q, k, v, gate]
+        args_lo[which], args_hi[which] = lo, hi
+        num = (loss(*args_hi) - loss(*args_lo)) / (float(hi[pos]) - float(lo[pos]))
+        assert abs(num - analytic) <= 1e-5 * max(1.0, abs(analytic)), (which, pos, num, analytic)
+
+    for pos in [(3, 1, 2), (6, 0, 0), (0, 1, 3)]:
+        secant(q, pos, dq[pos], 0)
+    for pos in [(0, 1), (2, 3), (5, 0)]:
+        secant(k, pos, dk[pos], 1)
+        secant(v, pos, dv[pos], 2)
+    for pos in [(4, 1), (6, 0)]:
+        secant(gate, pos, dg[pos], 3)
+
+
+def test_backward_single_key_closed_form():
+    # one selected key: p = 1, so the logits get no gradient and dv = g * dout
+    d, Hq = 4, 2
+    q, k, v = _rand((1, Hq, d), 60), _rand((3, d), 61), _rand((3, d), 62)
+    gate, dout = _rand((1, Hq), 63), _rand((1, Hq, d), 64)
+    idx = np.array([[2, -1]], dtype=np.int32)
+    dq, dk, dv, dg = oracle.attend_backward(q, k, v, d, d, d, gate, [0], [0], idx, 1.0, dout, n_keys=3)
+    g = 1 / (1 + np.exp(-gate.double().numpy()[0]))
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15      # zero up to rounding
+    np.testing.assert_allclose(dv[2], (g[:, None] * dout.double().numpy()[0]).sum(0), rtol=1e-14)
+    assert np.all(dv[:2] == 0)
+    np.testing.assert_allclose(dg[0], g * (1 - g) * (dout.double().numpy()[0] * v[2].double().numpy()).sum(-1),
+                               rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
 # the composed layer
 # ---------------------------------------------------------------------------
 
