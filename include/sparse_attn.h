@@ -212,6 +212,48 @@ SA_API size_t sa_decode_workspace_size(const sa_decode_args* args);
 SA_API int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/*
+ * Gradients of steps 3-4 over a fixed index set (the training path:
+ * "Hybrid Attention Architectures...", section 3.1 -- once the indexer has
+ * chosen the set, attention over it is ordinary softmax attention -- and
+ * section 3.3 -- the gate scales its output). For query row t of one causal
+ * sequence, with the positions idx[t, :] (entries < 0 skipped; the kept
+ * positions sparse_attn_prefill returns), l_i = softmax_scale * q_h . k_i,
+ * p = softmax(l), o_h = sum_i p_i v_i, out_h = sigmoid(gate_h) o_h, the call
+ * returns the derivatives of sum(dout * out):
+ *   dq [L, Hq, dqk], dgate [L, Hq] (with respect to the gate logits), and
+ *   dk [L, dqk], dv [L, dv]: each key / value row's total over every query
+ *   that selected it (overwritten; accumulated on the GPU in fp32 in an
+ *   order that varies from run to run).
+ * All outputs are fp32. Supported: dtype SA_BF16 or SA_F32 (q, k, v, dout),
+ * dqk == dv in {64, 128}, 1 <= Hq <= 16, ld_k >= dqk, ld_v >= dv (multiples
+ * of 8), v may alias k; 1 <= K <= 65536. The caller owns every buffer; the
+ * call allocates nothing and needs no workspace. Errors: SA_ERR_INVALID_ARG
+ * (null or misaligned pointers, bad sizes), SA_ERR_UNSUPPORTED (shapes above),
+ * SA_ERR_LAUNCH.
+ */
+typedef struct {
+    int L;                 /* query rows = key rows of the sequence           */
+    int Hq, dqk, dv;
+    int K;                 /* entries per row of idx                          */
+    int dtype;             /* SA_BF16 or SA_F32                               */
+    float softmax_scale;
+    const void* q;         /* [L, Hq, dqk]                                    */
+    const void* k;         /* [L, ld_k]                                       */
+    int64_t ld_k;
+    const void* v;         /* [L, ld_v]                                       */
+    int64_t ld_v;
+    const int32_t* idx;    /* [L, K] kept positions of each row, -1 = none    */
+    const float* gate;     /* [L, Hq] gate logits                             */
+    const void* dout;      /* [L, Hq, dv] gradient of the layer output        */
+    float* dq;             /* [L, Hq, dqk]                                    */
+    float* dk;             /* [L, dqk]                                        */
+    float* dv_out;         /* [L, dv]                                         */
+    float* dgate;          /* [L, Hq]                                         */
+} sa_backward_args;
+
+SA_API int sparse_attn_backward(const sa_backward_args* args, cudaStream_t stream);
+
 /* Bytes of device scratch the library carries for sparse_attn_decode_noalloc. */
 #define SA_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -44,6 +44,14 @@ class DecodeArgs(ctypes.Structure):
                 ("max_ctx", _I64), ("out", _P), ("idx_out", _P), ("stage_events", _P)]
 
 
+class BackwardArgs(ctypes.Structure):
+    """Mirror of sa_backward_args."""
+    _fields_ = [("L", _I), ("Hq", _I), ("dqk", _I), ("dv", _I), ("K", _I), ("dtype", _I),
+                ("softmax_scale", _F), ("q", _P), ("k", _P), ("ld_k", _I64), ("v", _P), ("ld_v", _I64),
+                ("idx", _P), ("gate", _P), ("dout", _P), ("dq", _P), ("dk", _P), ("dv_out", _P),
+                ("dgate", _P)]
+
+
 class SparseAttnError(RuntimeError):
     def __init__(self, fn: str, status: int):
         super().__init__(f"{fn}: {status_string(status)} ({status})")
@@ -80,6 +88,8 @@ def load_library(path: str | None = None):
     lib.sparse_attn_decode.restype = _I
     lib.sparse_attn_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), _P]
     lib.sparse_attn_decode_noalloc.restype = _I
+    lib.sparse_attn_backward.argtypes = [ctypes.POINTER(BackwardArgs), _P]
+    lib.sparse_attn_backward.restype = _I
     if path is None:
         _lib = lib
     return lib
@@ -214,6 +224,28 @@ def sparse_attn_prefill(q, k, v, q_idx, k_idx, w, gate, K: int, softmax_scale: f
                                  _stream(q.device, stream))
     _check("sparse_attn_prefill", st)
     return out
+
+
+def sparse_attn_backward(q, k, v, idx, gate, dout, softmax_scale: float, ld_k=None, ld_v=None,
+                         stream=None):
+    """Gradients of the gated attention of one causal sequence over the fixed
+    index set idx [L, K] (the kept positions of the forward). q [L, Hq, d];
+    k, v rows [L, ld]; dout [L, Hq, d] in q's dtype. Returns fp32 dq [L, Hq, d],
+    dk [L, d], dv [L, d] and dgate [L, Hq] (with respect to the gate logits)."""
+    L, Hq, d = q.shape
+    a = BackwardArgs()
+    a.L, a.Hq, a.dqk, a.dv, a.K = L, Hq, d, d, idx.shape[1]
+    a.dtype, a.softmax_scale = dtype_code(q.dtype), softmax_scale
+    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.ld_k = k.stride(0) if ld_k is None else ld_k
+    a.ld_v = v.stride(0) if ld_v is None else ld_v
+    a.idx, a.gate, a.dout = _ptr(idx), _ptr(gate), _ptr(dout)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dv, dg = (torch.empty((L, Hq, d), **f32), torch.empty((L, d), **f32), torch.empty((L, d), **f32),
+                      torch.empty((L, Hq), **f32))
+    a.dq, a.dk, a.dv_out, a.dgate = _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg)
+    _check("sparse_attn_backward", load_library().sparse_attn_backward(ctypes.byref(a), _stream(q.device, stream)))
+    return dq, dk, dv, dg
 
 
 def decode_args(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len, max_ctx: int,

@@ -422,6 +422,30 @@ int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, 
     return SA_OK;
 }
 
+int sparse_attn_backward(const sa_backward_args* args, cudaStream_t stream)
+{
+    if (!args) return SA_ERR_INVALID_ARG;
+    const sa_backward_args& a = *args;
+    if (a.L < 0 || a.Hq < 1 || a.dqk < 1 || a.dv < 1 || a.K < 1) return SA_ERR_INVALID_ARG;
+    if (a.dtype != SA_BF16 && a.dtype != SA_F32) return valid_dtype(a.dtype) ? SA_ERR_UNSUPPORTED : SA_ERR_INVALID_ARG;
+    if (a.ld_k < a.dqk || a.ld_v < a.dv) return SA_ERR_INVALID_ARG;
+    if (!(a.softmax_scale == a.softmax_scale)) return SA_ERR_INVALID_ARG;
+    if (a.dqk != a.dv || a.K > MAX_K || a.ld_k % 8 != 0 || a.ld_v % 8 != 0) return SA_ERR_UNSUPPORTED;
+    sa::BwdArgs b{};
+    b.L = a.L; b.Hq = a.Hq; b.D = a.dqk; b.K = a.K; b.dtype = a.dtype; b.softmax_scale = a.softmax_scale;
+    b.q = a.q; b.k = a.k; b.ld_k = a.ld_k; b.v = a.v; b.ld_v = a.ld_v; b.idx = a.idx; b.gate = a.gate;
+    b.dout = a.dout; b.dq = a.dq; b.dk = a.dk; b.dv = a.dv_out; b.dgate = a.dgate;
+    if (!sa::attention_backward_supported(b)) return SA_ERR_UNSUPPORTED;
+    if (a.L == 0) return SA_OK;
+    if (!a.q || !a.k || !a.v || !a.idx || !a.gate || !a.dout || !a.dq || !a.dk || !a.dv_out || !a.dgate)
+        return SA_ERR_INVALID_ARG;
+    if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.dout, 16) ||
+        !aligned(a.dk, 16) || !aligned(a.dv_out, 16) || !aligned(a.dq, 4) || !aligned(a.dgate, 4) ||
+        !aligned(a.gate, 4) || !aligned(a.idx, 4))
+        return SA_ERR_INVALID_ARG;
+    return status_of(sa::launch_attention_backward(b, stream));
+}
+
 size_t sa_decode_workspace_size(const sa_decode_args* args)
 {
     if (check_decode_scalars(args) != SA_OK) return 0;

@@ -142,6 +142,26 @@ cudaError_t launch_sample_threshold(const FusedSelectArgs& a, const float* ssc, 
 size_t fused_select_smem(const FusedSelectArgs& a);
 cudaError_t launch_fused_select(const FusedSelectArgs& a, cudaStream_t s);   // select + fallback
 
+// ---- gradients of steps 3-4 over a fixed index set -------------------------
+struct BwdArgs {
+    int L, Hq, D, K, dtype;  // D = dqk = dv
+    float softmax_scale;
+    const void* q;           // [L, Hq, D]
+    const void* k;           // row j at k + j * ld_k
+    int64_t ld_k;
+    const void* v;
+    int64_t ld_v;
+    const int32_t* idx;      // [L, K], < 0 = none
+    const float* gate;       // [L, Hq]
+    const void* dout;        // [L, Hq, D]
+    float* dq;               // [L, Hq, D]
+    float* dk;               // [L, D]
+    float* dv;               // [L, D]
+    float* dgate;            // [L, Hq]
+};
+bool attention_backward_supported(const BwdArgs& a);
+cudaError_t launch_attention_backward(const BwdArgs& a, cudaStream_t s);
+
 // ---- step 2: Top-K over score rows -----------------------------------------
 struct TopkArgs {
     const float* scores;    // row r at scores + r * ld_s

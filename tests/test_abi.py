@@ -60,7 +60,8 @@ def _c_offsets(struct, fields, tmp_path):
 
 
 @pytest.mark.parametrize("struct,mirror", [("sa_prefill_args", binding.PrefillArgs),
-                                           ("sa_decode_args", binding.DecodeArgs)])
+                                           ("sa_decode_args", binding.DecodeArgs),
+                                           ("sa_backward_args", binding.BackwardArgs)])
 def test_argument_structs_match_header(struct, mirror, tmp_path):
     fields = [f for f, _ in mirror._fields_]
     got = _c_offsets(struct, fields, tmp_path)
@@ -178,3 +179,27 @@ def test_standalone_argument_errors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         binding.load_library(str(tmp_path / "nope.so"))
+
+
+def _backward(**kw):
+    a = binding.BackwardArgs()
+    a.L, a.Hq, a.dqk, a.dv, a.K, a.dtype = 64, 16, 128, 128, 32, binding.SA_BF16
+    a.softmax_scale, a.ld_k, a.ld_v = 0.1, 128, 128
+    fake = 1 << 20                       # never dereferenced: every call here fails first
+    for f in ("q", "k", "v", "idx", "gate", "dout", "dq", "dk", "dv_out", "dgate"):
+        setattr(a, f, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=0), binding.SA_ERR_INVALID_ARG), (dict(K=0), binding.SA_ERR_INVALID_ARG),
+    (dict(dtype=7), binding.SA_ERR_INVALID_ARG), (dict(dtype=binding.SA_FP8_E4M3), binding.SA_ERR_UNSUPPORTED),
+    (dict(dqk=96, dv=96, ld_k=96, ld_v=96), binding.SA_ERR_UNSUPPORTED),
+    (dict(dv=64, ld_v=64), binding.SA_ERR_UNSUPPORTED), (dict(Hq=17), binding.SA_ERR_UNSUPPORTED),
+    (dict(ld_k=100), binding.SA_ERR_INVALID_ARG), (dict(dq=None), binding.SA_ERR_INVALID_ARG),
+    (dict(dk=(1 << 20) + 4), binding.SA_ERR_INVALID_ARG),
+])
+def test_backward_argument_errors(lib, kw, status):
+    assert lib.sparse_attn_backward(ctypes.byref(_backward(**kw)), None) == status
