@@ -13,7 +13,8 @@
 //           and dv = p^T do go to the key / value rows with fp32 vector
 //           atomics (a row is shared by every query that selected it).
 // fp32 arithmetic throughout on CUDA cores; inputs are converted once per
-// chunk into shared memory (rows padded by one word: conflict-free columns).
+// chunk into shared memory, and every product loop is register-blocked over
+// 16-byte shared-memory loads.
 #include "common.cuh"
 #include "kernels.h"
 #include "../../include/sparse_attn.h"
@@ -27,8 +28,8 @@ constexpr int BW_MAX_HQ = 16;
 
 template <int D>
 struct BwCfg {
-    static constexpr int LD = D + 1;                       // padded row of the chunk tiles
-    static constexpr int PER = BW_MAX_HQ * D / BW_THREADS; // (head, column) outputs per thread
+    static constexpr int LD = D + 4;                       // padded row of the chunk tiles (16-byte aligned)
+    static constexpr int TPH = D / 8;                      // dq: threads per head, 8 columns each
     static size_t smem(int Hq)
     {
         return sizeof(float) * ((size_t)3 * Hq * D + 2 * (size_t)BW_CH * LD + 2 * (size_t)Hq * (BW_CH + 1) + 6 * Hq);
@@ -54,8 +55,14 @@ SA_DEVINL void load8(const float* p, float* o)
     o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
+SA_DEVINL float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+SA_DEVINL float dot4(float4 a, float4 b, float s)
+{
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, s))));
+}
+
 template <int D, typename T>
-__global__ void __launch_bounds__(BW_THREADS)
+__global__ void __launch_bounds__(BW_THREADS, 3)
 attn_bwd_kernel(BwdArgs a)
 {
     using C = BwCfg<D>;
@@ -93,10 +100,11 @@ attn_bwd_kernel(BwdArgs a)
         m_s[h] = -INFINITY; l_s[h] = 0.0f; D_s[h] = 0.0f; dto_s[h] = 0.0f;
     }
 
-    // (head, column) outputs of this thread: index tid + BW_THREADS * k
-    float acc[C::PER];
+    // pass 1 output of this thread: head oh, columns od0 .. od0 + 7
+    const int oh = tid / C::TPH, od0 = (tid % C::TPH) * 8;
+    float oa[8];
 #pragma unroll
-    for (int k = 0; k < C::PER; ++k) acc[k] = 0.0f;
+    for (int u = 0; u < 8; ++u) oa[u] = 0.0f;
 
     // chunk loader: rows of k and v for kept entries c0 .. c0 + BW_CH - 1
     auto load_chunk = [&](int c0) {
@@ -126,12 +134,17 @@ attn_bwd_kernel(BwdArgs a)
     // ---------------- pass 1: the forward, online softmax ----------------
     for (int c0 = 0; c0 < a.K; c0 += BW_CH) {
         load_chunk(c0);
-        for (int p = tid; p < Hq * BW_CH; p += BW_THREADS) {
-            const int h = p / BW_CH, c = p % BW_CH;
-            float s = 0.0f;
-#pragma unroll 8
-            for (int d = 0; d < D; ++d) s = fmaf(qs[h * D + d], ks[c * C::LD + d], s);
-            ps[h * (BW_CH + 1) + c] = jrow[c] >= 0 ? s * a.softmax_scale : -INFINITY;
+        for (int p = tid; p < Hq * (BW_CH / 2); p += BW_THREADS) {   // rows c and c + 16 of head h
+            const int h = p / (BW_CH / 2), c = p % (BW_CH / 2);
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 4
+            for (int d = 0; d < D; d += 4) {
+                const float4 qv = lds4(qs + h * D + d);
+                s0 = dot4(qv, lds4(ks + c * C::LD + d), s0);
+                s1 = dot4(qv, lds4(ks + (c + 16) * C::LD + d), s1);
+            }
+            ps[h * (BW_CH + 1) + c] = jrow[c] >= 0 ? s0 * a.softmax_scale : -INFINITY;
+            ps[h * (BW_CH + 1) + c + 16] = jrow[c + 16] >= 0 ? s1 * a.softmax_scale : -INFINITY;
         }
         __syncthreads();
         for (int h = warp; h < Hq; h += BW_THREADS / 32) {        // one warp per head, lane = row
@@ -155,39 +168,39 @@ attn_bwd_kernel(BwdArgs a)
             }
         }
         __syncthreads();
+        // o = o * alpha + p v: this thread's head and 8 consecutive columns
+        if (oh < Hq) {
+            const float al = al_s[oh];
 #pragma unroll
-        for (int k = 0; k < C::PER; ++k) {
-            const int i = tid + BW_THREADS * k;
-            const int h = i / D, e = i % D;
-            if (h < Hq) {
-                float o = acc[k] * al_s[h];
-#pragma unroll 8
-                for (int c = 0; c < BW_CH; ++c) o = fmaf(ps[h * (BW_CH + 1) + c], vs[c * C::LD + e], o);
-                acc[k] = o;
+            for (int u = 0; u < 8; ++u) oa[u] *= al;
+#pragma unroll 4
+            for (int c = 0; c < BW_CH; ++c) {
+                const float w = ps[oh * (BW_CH + 1) + c];
+                const float4 v0 = lds4(vs + c * C::LD + od0), v1 = lds4(vs + c * C::LD + od0 + 4);
+                oa[0] = fmaf(w, v0.x, oa[0]); oa[1] = fmaf(w, v0.y, oa[1]);
+                oa[2] = fmaf(w, v0.z, oa[2]); oa[3] = fmaf(w, v0.w, oa[3]);
+                oa[4] = fmaf(w, v1.x, oa[4]); oa[5] = fmaf(w, v1.y, oa[5]);
+                oa[6] = fmaf(w, v1.z, oa[6]); oa[7] = fmaf(w, v1.w, oa[7]);
             }
         }
         __syncthreads();
     }
-    // o = acc / l; D_h = do . o; dout . o for the gate
-#pragma unroll
-    for (int k = 0; k < C::PER; ++k) {
-        const int i = tid + BW_THREADS * k;
-        const int h = i / D;
+    // o = oa / l; D_h = do . o; dout . o for the gate
+    if (oh < Hq) {
+        const float il = l_s[oh] > 0.0f ? 1.0f / l_s[oh] : 0.0f;
         float dsum = 0.0f, tsum = 0.0f;
-        if (h < Hq) {
-            const float o = l_s[h] > 0.0f ? acc[k] / l_s[h] : 0.0f;
-            dsum = dos[i] * o;
-            tsum = dos_raw[i] * o;
-        }
-        // a warp's 32 outputs share one head (D is a multiple of 32)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, o);
-            tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
+        for (int u = 0; u < 8; ++u) {
+            const float o = oa[u] * il;
+            dsum = fmaf(dos[oh * D + od0 + u], o, dsum);
+            tsum = fmaf(dos_raw[oh * D + od0 + u], o, tsum);
         }
-        if (lane == 0 && h < Hq) { atomicAdd(&D_s[h], dsum); atomicAdd(&dto_s[h], tsum); }
-        acc[k] = 0.0f;                          // reused for dq
+        atomicAdd(&D_s[oh], dsum);
+        atomicAdd(&dto_s[oh], tsum);
     }
+    float dqa[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) dqa[u] = 0.0f;
     __syncthreads();
     for (int h = tid; h < Hq; h += BW_THREADS) {
         lse_s[h] = m_s[h] == -INFINITY ? 0.0f : m_s[h] + __logf(l_s[h]);
@@ -199,56 +212,83 @@ attn_bwd_kernel(BwdArgs a)
     // ---------------- pass 2: gradients ----------------
     for (int c0 = 0; c0 < a.K; c0 += BW_CH) {
         load_chunk(c0);
-        for (int p = tid; p < Hq * BW_CH; p += BW_THREADS) {
-            const int h = p / BW_CH, c = p % BW_CH;
-            float s = 0.0f, dp = 0.0f;
-#pragma unroll 8
-            for (int d = 0; d < D; ++d) {
-                s = fmaf(qs[h * D + d], ks[c * C::LD + d], s);
-                dp = fmaf(dos[h * D + d], vs[c * C::LD + d], dp);
+        for (int p = tid; p < Hq * (BW_CH / 2); p += BW_THREADS) {   // rows c and c + 16 of head h
+            const int h = p / (BW_CH / 2), c = p % (BW_CH / 2);
+            float s0 = 0.0f, s1 = 0.0f, dp0 = 0.0f, dp1 = 0.0f;
+#pragma unroll 4
+            for (int d = 0; d < D; d += 4) {
+                const float4 qv = lds4(qs + h * D + d), dv4 = lds4(dos + h * D + d);
+                s0 = dot4(qv, lds4(ks + c * C::LD + d), s0);
+                s1 = dot4(qv, lds4(ks + (c + 16) * C::LD + d), s1);
+                dp0 = dot4(dv4, lds4(vs + c * C::LD + d), dp0);
+                dp1 = dot4(dv4, lds4(vs + (c + 16) * C::LD + d), dp1);
             }
-            const float pr = jrow[c] >= 0 ? __expf(s * a.softmax_scale - lse_s[h]) : 0.0f;
-            ps[h * (BW_CH + 1) + c] = pr;
-            dss[h * (BW_CH + 1) + c] = pr * (dp - D_s[h]);
+            const float p0 = jrow[c] >= 0 ? __expf(s0 * a.softmax_scale - lse_s[h]) : 0.0f;
+            const float p1 = jrow[c + 16] >= 0 ? __expf(s1 * a.softmax_scale - lse_s[h]) : 0.0f;
+            ps[h * (BW_CH + 1) + c] = p0;
+            ps[h * (BW_CH + 1) + c + 16] = p1;
+            dss[h * (BW_CH + 1) + c] = p0 * (dp0 - D_s[h]);
+            dss[h * (BW_CH + 1) + c + 16] = p1 * (dp1 - D_s[h]);
         }
         __syncthreads();
-        // dq += scale * ds k
-#pragma unroll
-        for (int k = 0; k < C::PER; ++k) {
-            const int i = tid + BW_THREADS * k;
-            const int h = i / D, d = i % D;
+        // dq += scale * ds k: this thread's head and 8 consecutive columns
+        {
+            const int h = tid / C::TPH, d0 = (tid % C::TPH) * 8;
             if (h < Hq) {
-                float g = acc[k];
-#pragma unroll 8
-                for (int c = 0; c < BW_CH; ++c) g = fmaf(dss[h * (BW_CH + 1) + c], ks[c * C::LD + d], g);
-                acc[k] = g;
+#pragma unroll 4
+                for (int c = 0; c < BW_CH; ++c) {
+                    const float w = dss[h * (BW_CH + 1) + c];
+                    const float4 k0 = lds4(ks + c * C::LD + d0), k1 = lds4(ks + c * C::LD + d0 + 4);
+                    dqa[0] = fmaf(w, k0.x, dqa[0]); dqa[1] = fmaf(w, k0.y, dqa[1]);
+                    dqa[2] = fmaf(w, k0.z, dqa[2]); dqa[3] = fmaf(w, k0.w, dqa[3]);
+                    dqa[4] = fmaf(w, k1.x, dqa[4]); dqa[5] = fmaf(w, k1.y, dqa[5]);
+                    dqa[6] = fmaf(w, k1.z, dqa[6]); dqa[7] = fmaf(w, k1.w, dqa[7]);
+                }
             }
         }
-        // this chunk's dk = scale ds^T q and dv = p^T do, four columns per atomic
-        for (int x = tid; x < BW_CH * (D / 4); x += BW_THREADS) {
-            const int c = x / (D / 4), d0 = (x % (D / 4)) * 4;
-            const int j = jrow[c];
-            if (j < 0) continue;
-            float4 gk = make_float4(0.f, 0.f, 0.f, 0.f), gv = make_float4(0.f, 0.f, 0.f, 0.f);
+        // this chunk's dk = scale ds^T q and dv = p^T do: a warp covers whole
+        // rows (four columns per lane, one coalesced 16-byte atomic per lane
+        // and row); a thread takes RPT rows
+        {
+            constexpr int LPR = D / 4;                 // lanes per row
+            constexpr int RPW = 32 / LPR;              // rows per warp and step
+            constexpr int RPT = BW_CH / (RPW * (BW_THREADS / 32));
+            const int d0 = (lane % LPR) * 4;
+            const int cbase = warp * RPW + lane / LPR;
+            float4 gk[RPT], gv[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) { gk[r] = make_float4(0.f, 0.f, 0.f, 0.f); gv[r] = gk[r]; }
             for (int h = 0; h < Hq; ++h) {
-                const float dsv = dss[h * (BW_CH + 1) + c], pv = ps[h * (BW_CH + 1) + c];
-                const float* qh = qs + h * D + d0;
-                const float* dh = dos + h * D + d0;
-                gk.x = fmaf(dsv, qh[0], gk.x); gk.y = fmaf(dsv, qh[1], gk.y);
-                gk.z = fmaf(dsv, qh[2], gk.z); gk.w = fmaf(dsv, qh[3], gk.w);
-                gv.x = fmaf(pv, dh[0], gv.x); gv.y = fmaf(pv, dh[1], gv.y);
-                gv.z = fmaf(pv, dh[2], gv.z); gv.w = fmaf(pv, dh[3], gv.w);
+                const float4 qv = lds4(qs + h * D + d0), dv4 = lds4(dos + h * D + d0);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int c = cbase + r * RPW * (BW_THREADS / 32);
+                    const float dsv = dss[h * (BW_CH + 1) + c], pv = ps[h * (BW_CH + 1) + c];
+                    gk[r].x = fmaf(dsv, qv.x, gk[r].x); gk[r].y = fmaf(dsv, qv.y, gk[r].y);
+                    gk[r].z = fmaf(dsv, qv.z, gk[r].z); gk[r].w = fmaf(dsv, qv.w, gk[r].w);
+                    gv[r].x = fmaf(pv, dv4.x, gv[r].x); gv[r].y = fmaf(pv, dv4.y, gv[r].y);
+                    gv[r].z = fmaf(pv, dv4.z, gv[r].z); gv[r].w = fmaf(pv, dv4.w, gv[r].w);
+                }
             }
-            gk.x *= a.softmax_scale; gk.y *= a.softmax_scale; gk.z *= a.softmax_scale; gk.w *= a.softmax_scale;
-            atomicAdd(reinterpret_cast<float4*>(a.dk + (int64_t)j * D + d0), gk);
-            atomicAdd(reinterpret_cast<float4*>(a.dv + (int64_t)j * D + d0), gv);
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int c = cbase + r * RPW * (BW_THREADS / 32);
+                const int j = jrow[c];
+                if (j < 0) continue;
+                const float sc = a.softmax_scale;
+                atomicAdd(reinterpret_cast<float4*>(a.dk + (int64_t)j * D + d0),
+                          make_float4(gk[r].x * sc, gk[r].y * sc, gk[r].z * sc, gk[r].w * sc));
+                atomicAdd(reinterpret_cast<float4*>(a.dv + (int64_t)j * D + d0), gv[r]);
+            }
         }
         __syncthreads();
     }
+    {
+        const int h = tid / C::TPH, d0 = (tid % C::TPH) * 8;
+        if (h < Hq) {
 #pragma unroll
-    for (int k = 0; k < C::PER; ++k) {
-        const int i = tid + BW_THREADS * k;
-        if (i < Hq * D) a.dq[(int64_t)t * Hq * D + i] = acc[k] * a.softmax_scale;
+            for (int u = 0; u < 8; ++u) a.dq[((int64_t)t * Hq + h) * D + d0 + u] = dqa[u] * a.softmax_scale;
+        }
     }
 }
 
