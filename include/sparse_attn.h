@@ -157,6 +157,25 @@ SA_API int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_
                         cudaStream_t stream);
 
 /*
+ * sparse_attn_prefill with block-granular selection (the block-level routing
+ * of "Sparse Attention and Hybrid Attention Architecture Design": keys are
+ * mean-pooled per block, the indexer scores blocks, Top-K keeps blocks, and
+ * exact attention runs inside the kept blocks). Blocks are block_size
+ * consecutive positions (block b = positions [b*bs, (b+1)*bs)); the pooled
+ * indexer key of a block is the mean of its k_idx rows rounded to bf16; query
+ * t scores the blocks holding a visible position (b*bs <= t), keeps the
+ * K / block_size best (ties: lower block), and attends over the positions
+ * <= t of the kept blocks. idx_out, if not NULL, receives [L, K] kept
+ * positions (ascending, -1 padded). With block_size 1 this is
+ * sparse_attn_prefill.
+ * Supported: idx_dtype SA_BF16; block_size a power of two in [1, 1024] that
+ * divides K; the other limits of sparse_attn_prefill.
+ */
+SA_API size_t sa_prefill_blocks_workspace_size(const sa_prefill_args* args, int block_size);
+SA_API int sparse_attn_prefill_blocks(const sa_prefill_args* args, int block_size, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/*
  * One decode step for B sequences: the new query of sequence b attends over
  * its ctx_len[b] cached rows, stored at packed rows seq_start[b] ..
  * seq_start[b] + ctx_len[b] - 1 of the caches (append the new token's own

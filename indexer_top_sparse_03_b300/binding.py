@@ -88,6 +88,10 @@ def load_library(path: str | None = None):
     lib.sparse_attn_decode.restype = _I
     lib.sparse_attn_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), _P]
     lib.sparse_attn_decode_noalloc.restype = _I
+    lib.sa_prefill_blocks_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs), _I]
+    lib.sa_prefill_blocks_workspace_size.restype = _SZ
+    lib.sparse_attn_prefill_blocks.argtypes = [ctypes.POINTER(PrefillArgs), _I, _P, _SZ, _P]
+    lib.sparse_attn_prefill_blocks.restype = _I
     lib.sparse_attn_backward.argtypes = [ctypes.POINTER(BackwardArgs), _P]
     lib.sparse_attn_backward.restype = _I
     if path is None:
@@ -223,6 +227,31 @@ def sparse_attn_prefill(q, k, v, q_idx, k_idx, w, gate, K: int, softmax_scale: f
     st = lib.sparse_attn_prefill(ctypes.byref(a), _ptr(ws), ws.numel() * ws.element_size(),
                                  _stream(q.device, stream))
     _check("sparse_attn_prefill", st)
+    return out
+
+
+def sparse_attn_prefill_blocks(q, k, v, q_idx, k_idx, w, gate, K: int, softmax_scale: float, block_size: int,
+                               ld_k=None, ld_v=None, dv=None, out=None, idx_out=None, workspace=None, stream=None,
+                               stage_events=None):
+    """sparse_attn_prefill with block-granular selection: K / block_size blocks
+    of block_size positions kept per query (bf16 indexer inputs)."""
+    L, Hq, dqk = q.shape
+    ld_k = k.stride(0) if ld_k is None else ld_k
+    ld_v = v.stride(0) if ld_v is None else ld_v
+    dv = (v.shape[-1] if v is not k else dqk) if dv is None else dv
+    if out is None:
+        out = torch.empty((L, Hq, dv), dtype=q.dtype, device=q.device)
+    a = _prefill_args(q, k, v, q_idx, k_idx, w, gate, K, softmax_scale, None, None, out, idx_out, ld_k, ld_v, dv)
+    ev = _events(stage_events)
+    a.stage_events = ctypes.cast(ev, ctypes.c_void_p).value if ev is not None else None
+    lib = load_library()
+    nbytes = lib.sa_prefill_blocks_workspace_size(ctypes.byref(a), block_size)
+    if nbytes == 0:
+        _check("sparse_attn_prefill_blocks", lib.sparse_attn_prefill_blocks(ctypes.byref(a), block_size, None, 0, None))
+    ws = _workspace(q.device, nbytes, workspace)
+    st = lib.sparse_attn_prefill_blocks(ctypes.byref(a), block_size, _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(q.device, stream))
+    _check("sparse_attn_prefill_blocks", st)
     return out
 
 

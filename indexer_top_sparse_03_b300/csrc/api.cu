@@ -275,6 +275,55 @@ int check_decode(const sa_decode_args* a)
     return SA_OK;
 }
 
+// ---- block-granular prefill ------------------------------------------------
+// pooled keys | block scores of one pass | block row lengths | kept blocks |
+// kept positions (if not returned) | kept-position counts
+struct BlocksLayout {
+    int lg;
+    int64_t nb, ld_b, rows_per_pass;
+    size_t pooled_off, scores_off, rowlen_off, blk_off, idx_off, cnt_off, total;
+};
+
+int block_lg(int block_size)
+{
+    if (block_size < 1 || block_size > 1024 || (block_size & (block_size - 1))) return -1;
+    int lg = 0;
+    while ((1 << lg) < block_size) ++lg;
+    return lg;
+}
+
+BlocksLayout blocks_layout(const sa_prefill_args& a, int lg)
+{
+    BlocksLayout l{};
+    l.lg = lg;
+    l.nb = ((int64_t)a.L + (1 << lg) - 1) >> lg;
+    l.ld_b = (l.nb + 3) / 4 * 4;
+    int64_t rows = (int64_t(1) << 30) / (4 * (l.ld_b > 0 ? l.ld_b : 4));
+    l.rows_per_pass = rows < 1 ? 1 : (rows > a.L ? a.L : rows);
+    const int Kb = a.K >> lg;
+    size_t off = 0;
+    l.pooled_off = off; off += align_up(sizeof(uint16_t) * (size_t)l.nb * a.di);
+    l.scores_off = off; off += align_up(sizeof(float) * (size_t)l.rows_per_pass * l.ld_b);
+    l.rowlen_off = off; off += align_up(sizeof(int32_t) * (size_t)l.rows_per_pass);
+    l.blk_off = off; off += align_up(sizeof(int32_t) * (size_t)l.rows_per_pass * Kb);
+    l.idx_off = off;
+    if (a.idx_out == nullptr) off += align_up(sizeof(int32_t) * (size_t)a.L * a.K);
+    l.cnt_off = off; off += align_up(sizeof(int32_t) * (size_t)a.L);
+    l.total = off;
+    return l;
+}
+
+int check_blocks(const sa_prefill_args* a, int block_size, bool scalars_only)
+{
+    int st = scalars_only ? check_prefill_scalars(a) : check_prefill(a);
+    if (st != SA_OK) return st;
+    const int lg = block_lg(block_size);
+    if (lg < 0) return SA_ERR_INVALID_ARG;
+    if (a->K % block_size != 0) return SA_ERR_INVALID_ARG;
+    if (a->idx_dtype != SA_BF16) return SA_ERR_UNSUPPORTED;
+    return SA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -444,6 +493,61 @@ int sparse_attn_backward(const sa_backward_args* args, cudaStream_t stream)
         !aligned(a.gate, 4) || !aligned(a.idx, 4))
         return SA_ERR_INVALID_ARG;
     return status_of(sa::launch_attention_backward(b, stream));
+}
+
+size_t sa_prefill_blocks_workspace_size(const sa_prefill_args* args, int block_size)
+{
+    if (check_blocks(args, block_size, true) != SA_OK) return 0;
+    return blocks_layout(*args, block_lg(block_size)).total;
+}
+
+int sparse_attn_prefill_blocks(const sa_prefill_args* args, int block_size, void* ws, size_t ws_bytes,
+                               cudaStream_t stream)
+{
+    int st = check_blocks(args, block_size, false);
+    if (st != SA_OK) return st;
+    const sa_prefill_args& a = *args;
+    if (a.L == 0) return SA_OK;
+    const BlocksLayout lay = blocks_layout(a, block_lg(block_size));
+    if (!ws || ws_bytes < lay.total || !aligned(ws, WS_ALIGN)) return SA_ERR_WORKSPACE;
+    char* wsb = static_cast<char*>(ws);
+    void* pooled = wsb + lay.pooled_off;
+    float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
+    int32_t* rowlen = reinterpret_cast<int32_t*>(wsb + lay.rowlen_off);
+    int32_t* blk = reinterpret_cast<int32_t*>(wsb + lay.blk_off);
+    int32_t* idx = a.idx_out ? a.idx_out : reinterpret_cast<int32_t*>(wsb + lay.idx_off);
+    int32_t* cnt = reinterpret_cast<int32_t*>(wsb + lay.cnt_off);
+    const int Kb = a.K >> lay.lg;
+
+    if (sa::launch_pool_keys(a.k_idx, a.L, a.di, lay.lg, pooled, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    for (int64_t t0 = 0; t0 < a.L; t0 += lay.rows_per_pass) {
+        const int64_t t1 = (t0 + lay.rows_per_pass < a.L) ? t0 + lay.rows_per_pass : a.L;
+        const int rows = (int)(t1 - t0);
+        sa::IndexerArgs ia{};
+        ia.q_idx = a.q_idx; ia.dtype = a.idx_dtype; ia.w = a.w;
+        ia.k_idx = pooled; ia.T = (int)t1; ia.N = (int)lay.nb; ia.Hi = a.Hi; ia.di = a.di;
+        ia.t_begin = (int)t0; ia.scores = scores; ia.ld_s = lay.ld_b; ia.block_log2 = lay.lg;
+        if (sa::launch_indexer(ia, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+        if (sa::launch_block_rowlen(t0, rows, lay.lg, rowlen, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+        sa::TopkArgs ta{};
+        ta.scores = scores; ta.ld_s = lay.ld_b; ta.row_len = rowlen; ta.n_cap = lay.nb;
+        ta.rows = rows; ta.K = Kb; ta.idx = blk; ta.ld_idx = Kb;
+        if (sa::launch_topk(ta, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+        if (sa::launch_expand_blocks(blk, Kb, t0, rows, lay.lg, idx + t0 * a.K, cnt + t0, stream) != cudaSuccess)
+            return SA_ERR_LAUNCH;
+    }
+    if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    sa::AttnArgs at{};
+    at.q = a.q; at.k = a.k; at.ld_k = a.ld_k; at.v = a.v; at.ld_v = a.ld_v;
+    at.v_aliases_k = (a.v == a.k) && a.ld_v == a.ld_k;
+    at.row_base = nullptr; at.idx = idx; at.K = a.K; at.ctx_len = nullptr; at.kept_len = cnt;
+    at.causal_first = 0; at.n_cap = a.L; at.gate = a.gate;
+    at.rows = a.L; at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
+    at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype; at.out = a.out;
+    at.splits = 1; at.part = nullptr; at.tickets = nullptr;
+    if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (a.stage_events && cudaEventRecord(a.stage_events[1], stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    return SA_OK;
 }
 
 size_t sa_decode_workspace_size(const sa_decode_args* args)

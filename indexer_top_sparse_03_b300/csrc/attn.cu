@@ -52,7 +52,7 @@ attn_mma_kernel(AttnArgs a)
     const int vld = a.v_aliases_k ? ks_ld : vs_ld;
 
     const int64_t n = attn_hist_len(a, r);
-    const int n_sel = (int)min64(a.K, n);
+    const int n_sel = attn_kept(a, r, n);
     const int per = (a.K + a.splits - 1) / a.splits;
     const int begin = min(split * per, n_sel), end = min(begin + per, n_sel);
     const int cnt = end - begin;
@@ -261,7 +261,7 @@ attn_simt_kernel(AttnArgs a)
     for (int d = tid; d < dqk; d += AT_THREADS) qsh[d] = to_f32(q[d]);
 
     const int64_t n = attn_hist_len(a, r);
-    const int n_sel = (int)min64(a.K, n);
+    const int n_sel = attn_kept(a, r, n);
     const int per = (a.K + a.splits - 1) / a.splits;
     const int begin = min(split * per, n_sel), end = min(begin + per, n_sel);
     const int64_t base = attn_base(a, r);

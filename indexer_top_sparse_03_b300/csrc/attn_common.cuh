@@ -18,6 +18,13 @@ SA_DEVINL int64_t attn_hist_len(const AttnArgs& a, int r)
 
 SA_DEVINL int64_t attn_base(const AttnArgs& a, int r) { return a.row_base ? a.row_base[r] : 0; }
 
+// entries of idx row r that hold kept positions (all at the front)
+SA_DEVINL int attn_kept(const AttnArgs& a, int r, int64_t n)
+{
+    const int64_t k = a.kept_len ? (int64_t)a.kept_len[r] : n;
+    return (int)min64(a.K, k < 0 ? 0 : (k > n ? n : k));
+}
+
 SA_DEVINL float gate_of(const AttnArgs& a, int r, int h)
 {
     const float x = a.gate[(int64_t)r * a.Hq + h];

@@ -66,7 +66,7 @@ attn_gather_kernel(AttnArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3, mat = lane >> 3, rr = lane & 7;
     const int64_t n = attn_hist_len(a, r);
-    const int n_sel = (int)min64(a.K, n);
+    const int n_sel = attn_kept(a, r, n);
     const int per = (a.K + a.splits - 1) / a.splits;
     const int begin = min(split * per, n_sel), end = min(begin + per, n_sel);
     const int cnt = end - begin;

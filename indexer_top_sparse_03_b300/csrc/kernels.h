@@ -57,6 +57,9 @@ struct IndexerArgs {
     // sampled keys: k_idx row i is the key sampled from stratum i (see
     // sample_pos); then n_t = min(N, sample_count(t)) instead of the causal n_t
     int sample_log2;        // 0: off
+    // pooled keys: k_idx row b is the mean of positions [b 2^lg, (b+1) 2^lg);
+    // then n_t = min(N, (t >> lg) + 1): every block holding a visible position
+    int block_log2;         // 0: off
     // filter mode (thr != null): no score is stored; a (query t, key j) pair
     // with score_key(s) >= thr[t - t_begin] is appended, as the composite
     // (score_key << 32 | ~j), to the segment of its work item: segment g of
@@ -99,7 +102,8 @@ __host__ __device__ inline int64_t sample_count(int64_t t, int lg)
 // keys visible to query row t
 __host__ __device__ inline int64_t indexer_row_n(const IndexerArgs& a, int64_t t)
 {
-    const int64_t n = a.sample_log2 ? sample_count(t, a.sample_log2) : t + 1 + a.causal_offset;
+    const int64_t n = a.sample_log2 ? sample_count(t, a.sample_log2)
+                    : a.block_log2 ? (t < 0 ? 0 : (t >> a.block_log2) + 1) : t + 1 + a.causal_offset;
     return n < 0 ? 0 : (n > a.N ? a.N : n);
 }
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);        // picks one of:
@@ -141,6 +145,16 @@ cudaError_t launch_sample_threshold(const FusedSelectArgs& a, const float* ssc, 
                                     cudaStream_t s);
 size_t fused_select_smem(const FusedSelectArgs& a);
 cudaError_t launch_fused_select(const FusedSelectArgs& a, cudaStream_t s);   // select + fallback
+
+// ---- block-granular selection -----------------------------------------------
+// mean of each block of 2^lg consecutive key rows (bf16 in, bf16 out, fp32 sum)
+cudaError_t launch_pool_keys(const void* k_idx, int64_t N, int di, int lg, void* pooled, cudaStream_t s);
+// n_r = ((t0 + r) >> lg) + 1 for rows r < rows
+cudaError_t launch_block_rowlen(int64_t t0, int rows, int lg, int32_t* row_len, cudaStream_t s);
+// selected blocks (ascending, -1 padded, Kb per row) -> their positions <= t,
+// ascending, -1 padded, Kb << lg per row; count[r] = positions written
+cudaError_t launch_expand_blocks(const int32_t* blk, int Kb, int64_t t0, int rows, int lg, int32_t* idx,
+                                 int32_t* count, cudaStream_t s);
 
 // ---- gradients of steps 3-4 over a fixed index set -------------------------
 struct BwdArgs {
@@ -187,6 +201,7 @@ struct AttnArgs {
     const int32_t* idx;     // [rows, K] kept positions, ascending, -1 padded
     int K;
     const int32_t* ctx_len; // [rows] history length per row, or null: n = causal_first + r + 1
+    const int32_t* kept_len;  // [rows] kept entries per row, or null: min(K, n)
     int64_t causal_first;
     int64_t n_cap;
     const float* gate;      // [rows, Hq]

@@ -28,6 +28,8 @@ Layer steps and where the pages state them:
               the first page returns gate * attn_out).
   attend_backward -- the gradients of the gated attention over a fixed
               index set (the training path), by the chain rule.
+  prefill_blocks_layer -- block-level routing: mean-pooled keys per block,
+              blocks scored and selected, attention inside the kept blocks.
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -247,6 +249,40 @@ def prefill_layer(inp, K: int, scale: float, rows=None, nthreads: int = 0):
     out = attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], dv, inp["gate"],
                  rows, np.zeros_like(rows), idx, scale, nthreads)
     return dict(rows=rows, scores=scores, idx=idx, out=out)
+
+
+def pool_keys_bf16(k_idx, block: int):
+    """Block-level routing's pooled keys ("Sparse Attention and Hybrid
+    Attention Architecture Design", block-level routing: keys mean-pooled per
+    block): the mean of each block of `block` consecutive rows (a last short
+    block averages the rows it has), evaluated in float64 from the stored bf16
+    values and stored as bf16 (round to nearest even, through float32)."""
+    kf = k_idx.double()
+    N = kf.shape[0]
+    nb = (N + block - 1) // block
+    means = torch.stack([kf[b * block:min(N, (b + 1) * block)].mean(dim=0) for b in range(nb)])
+    return means.float().to(torch.bfloat16).contiguous()
+
+
+def prefill_blocks_layer(inp, K: int, block: int, scale: float, rows=None, nthreads: int = 0):
+    """Block-granular causal prefill: query t scores the blocks b with
+    b * block <= t through their pooled keys (the indexer formula above),
+    keeps the K // block best (ties: lower block), and attends over the
+    positions <= t of the kept blocks. Returns the blocks' scores, the kept
+    blocks, the kept positions (ascending, -1 padded to K) and the output."""
+    L = inp["q"].shape[0]
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    pooled = pool_keys_bf16(inp["k_idx"], block)
+    nblk = rows // block + 1
+    scores = indexer(inp["q_idx"], inp["w"], pooled, rows, np.zeros_like(rows), nblk, nthreads=nthreads)
+    blk = topk(scores, K // block, nthreads=nthreads)
+    idx = np.full((len(rows), K), -1, dtype=np.int32)
+    for i, t in enumerate(rows):
+        pos = [p for b in sorted(x for x in blk[i] if x >= 0) for p in range(b * block, (b + 1) * block) if p <= t]
+        idx[i, :len(pos)] = pos
+    out = attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], inp["v"].shape[-1], inp["gate"], rows,
+                 np.zeros_like(rows), idx, scale, nthreads=nthreads)
+    return dict(rows=rows, scores=scores, blocks=blk, idx=idx, out=out)
 
 
 def decode_layer(inp, K: int, dv: int, scale: float, seqs=None, nthreads: int = 0):

@@ -203,3 +203,21 @@ def _backward(**kw):
 ])
 def test_backward_argument_errors(lib, kw, status):
     assert lib.sparse_attn_backward(ctypes.byref(_backward(**kw)), None) == status
+
+
+@pytest.mark.parametrize("bs,kw,status", [
+    (0, {}, binding.SA_ERR_INVALID_ARG), (48, {}, binding.SA_ERR_INVALID_ARG),
+    (2048, dict(K=4096), binding.SA_ERR_INVALID_ARG), (64, dict(K=96), binding.SA_ERR_INVALID_ARG),
+    (16, dict(idx_dtype=binding.SA_FP8_E4M3, q_scale=1 << 20, k_scale=1 << 20), binding.SA_ERR_UNSUPPORTED),
+])
+def test_blocks_argument_errors(lib, bs, kw, status):
+    a = _prefill(**kw)
+    assert lib.sa_prefill_blocks_workspace_size(ctypes.byref(a), bs) == 0
+    assert lib.sparse_attn_prefill_blocks(ctypes.byref(a), bs, None, 0, None) == status
+
+
+def test_blocks_workspace(lib):
+    a = _prefill()
+    n = lib.sa_prefill_blocks_workspace_size(ctypes.byref(a), 16)
+    assert n > 0 and n % 256 == 0
+    assert lib.sparse_attn_prefill_blocks(ctypes.byref(a), 16, None, 0, None) == binding.SA_ERR_WORKSPACE

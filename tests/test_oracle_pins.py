@@ -450,3 +450,40 @@ def test_thread_count_report():
     assert oracle.threads_used(3, 100) == 3
     assert oracle.threads_used(8, 2) == 2
     assert oracle.threads_used(0, 10 ** 6) >= 1
+
+
+# ---------------------------------------------------------------------------
+# block-level routing
+# ---------------------------------------------------------------------------
+
+def test_pooled_keys_are_block_means():
+    k = torch.tensor([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0], [7.0, 8.0], [-2.0, 0.5]]).to(torch.bfloat16)
+    p = oracle.pool_keys_bf16(k, 2)
+    assert p.dtype == torch.bfloat16
+    assert p.float().tolist() == [[2.0, 3.0], [6.0, 7.0], [-2.0, 0.5]]      # last block: its one row
+    same = torch.full((8, 4), 0.375).to(torch.bfloat16)
+    assert torch.equal(oracle.pool_keys_bf16(same, 4), same[:2])
+
+
+def test_blocks_of_one_position_are_the_token_path():
+    from workloads import get_config, make_prefill
+    cfg = get_config("prefill_8k", L=90, K=16, Hq=2)
+    inp = make_prefill(cfg, seed=5)
+    scale = 1 / math.sqrt(cfg.dqk)
+    tok = oracle.prefill_layer(inp, cfg.K, scale)
+    blk = oracle.prefill_blocks_layer(inp, cfg.K, 1, scale)
+    assert np.array_equal(np.sort(np.where(tok["idx"] < 0, 1 << 30, tok["idx"]), axis=1),
+                          np.where(blk["idx"] < 0, 1 << 30, blk["idx"]))
+    np.testing.assert_allclose(tok["out"], blk["out"], rtol=1e-13, atol=1e-16)   # summation order differs
+
+
+def test_blocks_covering_the_history_give_full_causal_attention():
+    from workloads import get_config, make_prefill
+    cfg = get_config("prefill_8k", L=70, K=128, Hq=2)
+    inp = make_prefill(cfg, seed=6)
+    scale = 1 / math.sqrt(cfg.dqk)
+    res = oracle.prefill_blocks_layer(inp, cfg.K, 16, scale)          # 8 blocks kept >= every row's 5
+    ref = _torch_gated_causal(inp["q"], inp["k"], inp["v"], inp["gate"], scale).numpy()
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-13)
+    for i, t in enumerate(res["rows"]):
+        assert res["idx"][i].tolist() == list(range(t + 1)) + [-1] * (cfg.K - t - 1)
