@@ -176,6 +176,19 @@ SA_API int sparse_attn_prefill_blocks(const sa_prefill_args* args, int block_siz
                                       cudaStream_t stream);
 
 /*
+ * sparse_attn_prefill fused with a sliding-window local branch (the branch
+ * fusion of "Sparse Attention and Hybrid Attention Architecture Design":
+ * out = g * sparse + (1 - g) * local, g = sigmoid(gate logit) per (token,
+ * head)). sparse is the pre-gate output of sparse_attn_prefill; local is
+ * exact attention of query t over positions max(0, t - window + 1) .. t.
+ * Supported: attn_dtype SA_BF16, window >= 1; the limits of
+ * sparse_attn_prefill. ws: at least sa_prefill_local_workspace_size bytes.
+ */
+SA_API size_t sa_prefill_local_workspace_size(const sa_prefill_args* args, int window);
+SA_API int sparse_attn_prefill_local(const sa_prefill_args* args, int window, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
+
+/*
  * One decode step for B sequences: the new query of sequence b attends over
  * its ctx_len[b] cached rows, stored at packed rows seq_start[b] ..
  * seq_start[b] + ctx_len[b] - 1 of the caches (append the new token's own

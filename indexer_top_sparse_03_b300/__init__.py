@@ -5,7 +5,8 @@ library; torch supplies device memory and streams only."""
 from .binding import (  # noqa: F401
     SA_BF16, SA_F32, SA_FP8_E4M3, SA_OK, SparseAttnError, decode_args, decode_workspace_size,
     dtype_code, indexer_score, load_library, sparse_attn_decode, sparse_attn_prefill,
-    sparse_attn_decode_noalloc, sparse_attn_backward, sparse_attn_prefill_blocks, status_string, topk_select,
+    sparse_attn_decode_noalloc, sparse_attn_backward, sparse_attn_prefill_blocks, sparse_attn_prefill_local, status_string,
+    topk_select,
 )
 
 __version__ = "0.1.0"

@@ -92,6 +92,10 @@ def load_library(path: str | None = None):
     lib.sa_prefill_blocks_workspace_size.restype = _SZ
     lib.sparse_attn_prefill_blocks.argtypes = [ctypes.POINTER(PrefillArgs), _I, _P, _SZ, _P]
     lib.sparse_attn_prefill_blocks.restype = _I
+    lib.sa_prefill_local_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs), _I]
+    lib.sa_prefill_local_workspace_size.restype = _SZ
+    lib.sparse_attn_prefill_local.argtypes = [ctypes.POINTER(PrefillArgs), _I, _P, _SZ, _P]
+    lib.sparse_attn_prefill_local.restype = _I
     lib.sparse_attn_backward.argtypes = [ctypes.POINTER(BackwardArgs), _P]
     lib.sparse_attn_backward.restype = _I
     if path is None:
@@ -252,6 +256,31 @@ def sparse_attn_prefill_blocks(q, k, v, q_idx, k_idx, w, gate, K: int, softmax_s
     st = lib.sparse_attn_prefill_blocks(ctypes.byref(a), block_size, _ptr(ws), ws.numel() * ws.element_size(),
                                         _stream(q.device, stream))
     _check("sparse_attn_prefill_blocks", st)
+    return out
+
+
+def sparse_attn_prefill_local(q, k, v, q_idx, k_idx, w, gate, K: int, softmax_scale: float, window: int,
+                              q_scale=None, k_scale=None, ld_k=None, ld_v=None, dv=None, out=None, idx_out=None,
+                              workspace=None, stream=None):
+    """sparse_attn_prefill fused with a sliding-window local branch:
+    out = g * sparse + (1 - g) * local, local = attention over the last
+    `window` positions (bf16 attention)."""
+    L, Hq, dqk = q.shape
+    ld_k = k.stride(0) if ld_k is None else ld_k
+    ld_v = v.stride(0) if ld_v is None else ld_v
+    dv = (v.shape[-1] if v is not k else dqk) if dv is None else dv
+    if out is None:
+        out = torch.empty((L, Hq, dv), dtype=q.dtype, device=q.device)
+    a = _prefill_args(q, k, v, q_idx, k_idx, w, gate, K, softmax_scale, q_scale, k_scale, out, idx_out, ld_k, ld_v,
+                      dv)
+    lib = load_library()
+    nbytes = lib.sa_prefill_local_workspace_size(ctypes.byref(a), window)
+    if nbytes == 0:
+        _check("sparse_attn_prefill_local", lib.sparse_attn_prefill_local(ctypes.byref(a), window, None, 0, None))
+    ws = _workspace(q.device, nbytes, workspace)
+    st = lib.sparse_attn_prefill_local(ctypes.byref(a), window, _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream(q.device, stream))
+    _check("sparse_attn_prefill_local", st)
     return out
 
 

@@ -550,6 +550,57 @@ int sparse_attn_prefill_blocks(const sa_prefill_args* args, int block_size, void
     return SA_OK;
 }
 
+size_t sa_prefill_local_workspace_size(const sa_prefill_args* args, int window)
+{
+    if (check_prefill_scalars(args) != SA_OK || window < 1 || args->attn_dtype != SA_BF16) return 0;
+    const sa_prefill_args& a = *args;
+    size_t off = prefill_layout(a).total;
+    off += align_up(sizeof(int32_t) * (size_t)a.L * window);            // window positions
+    off += align_up(sizeof(int32_t) * (size_t)a.L);                     // their counts
+    off += align_up(sizeof(float) * (size_t)a.L * a.Hq);                // negated gate logits
+    off += align_up(sizeof(uint16_t) * (size_t)a.L * a.Hq * a.dv);      // the local branch's output
+    return off;
+}
+
+int sparse_attn_prefill_local(const sa_prefill_args* args, int window, void* ws, size_t ws_bytes,
+                              cudaStream_t stream)
+{
+    int st = check_prefill(args);
+    if (st != SA_OK) return st;
+    if (window < 1) return SA_ERR_INVALID_ARG;
+    if (args->attn_dtype != SA_BF16) return SA_ERR_UNSUPPORTED;
+    const sa_prefill_args& a = *args;
+    if (a.L == 0) return SA_OK;
+    const size_t need = sa_prefill_local_workspace_size(args, window);
+    if (!ws || ws_bytes < need || !aligned(ws, WS_ALIGN)) return SA_ERR_WORKSPACE;
+    // the sparse branch, gated by g
+    const size_t base = prefill_layout(a).total;
+    st = sparse_attn_prefill(args, ws, base, stream);
+    if (st != SA_OK) return st;
+    char* wsb = static_cast<char*>(ws) + base;
+    int32_t* widx = reinterpret_cast<int32_t*>(wsb);
+    wsb += align_up(sizeof(int32_t) * (size_t)a.L * window);
+    int32_t* wcnt = reinterpret_cast<int32_t*>(wsb);
+    wsb += align_up(sizeof(int32_t) * (size_t)a.L);
+    float* neg = reinterpret_cast<float*>(wsb);
+    wsb += align_up(sizeof(float) * (size_t)a.L * a.Hq);
+    void* local = wsb;
+    // the local branch, gated by 1 - g = sigmoid(-x), then the sum
+    if (sa::launch_window_idx(0, a.L, window, widx, wcnt, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (sa::launch_negate(a.gate, neg, (int64_t)a.L * a.Hq, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    sa::AttnArgs at{};
+    at.q = a.q; at.k = a.k; at.ld_k = a.ld_k; at.v = a.v; at.ld_v = a.ld_v;
+    at.v_aliases_k = (a.v == a.k) && a.ld_v == a.ld_k;
+    at.row_base = nullptr; at.idx = widx; at.K = window; at.ctx_len = nullptr; at.kept_len = wcnt;
+    at.causal_first = 0; at.n_cap = a.L; at.gate = neg;
+    at.rows = a.L; at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
+    at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype; at.out = local;
+    at.splits = 1; at.part = nullptr; at.tickets = nullptr;
+    if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (sa::launch_add_bf16(a.out, local, (int64_t)a.L * a.Hq * a.dv, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    return SA_OK;
+}
+
 size_t sa_decode_workspace_size(const sa_decode_args* args)
 {
     if (check_decode_scalars(args) != SA_OK) return 0;

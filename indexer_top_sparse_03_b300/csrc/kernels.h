@@ -156,6 +156,15 @@ cudaError_t launch_block_rowlen(int64_t t0, int rows, int lg, int32_t* row_len, 
 cudaError_t launch_expand_blocks(const int32_t* blk, int Kb, int64_t t0, int rows, int lg, int32_t* idx,
                                  int32_t* count, cudaStream_t s);
 
+// ---- sliding-window local branch ---------------------------------------------
+// idx[r] = positions max(0, t - W + 1) .. t (t = t0 + r), ascending, W per row
+// (-1 padded); kept[r] = their count
+cudaError_t launch_window_idx(int64_t t0, int rows, int W, int32_t* idx, int32_t* kept, cudaStream_t s);
+// neg[i] = -x[i] (sigmoid(-x) = 1 - sigmoid(x))
+cudaError_t launch_negate(const float* x, float* neg, int64_t n, cudaStream_t s);
+// out[i] = round(out[i] + add[i]) for n bf16 elements (fp32 sum)
+cudaError_t launch_add_bf16(void* out, const void* add, int64_t n, cudaStream_t s);
+
 // ---- gradients of steps 3-4 over a fixed index set -------------------------
 struct BwdArgs {
     int L, Hq, D, K, dtype;  // D = dqk = dv

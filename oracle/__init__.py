@@ -30,6 +30,8 @@ Layer steps and where the pages state them:
               index set (the training path), by the chain rule.
   prefill_blocks_layer -- block-level routing: mean-pooled keys per block,
               blocks scored and selected, attention inside the kept blocks.
+  prefill_local_layer -- branch fusion with a sliding-window local branch,
+              g * sparse + (1 - g) * local.
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -283,6 +285,27 @@ def prefill_blocks_layer(inp, K: int, block: int, scale: float, rows=None, nthre
     out = attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], inp["v"].shape[-1], inp["gate"], rows,
                  np.zeros_like(rows), idx, scale, nthreads=nthreads)
     return dict(rows=rows, scores=scores, blocks=blk, idx=idx, out=out)
+
+
+def prefill_local_layer(inp, K: int, window: int, scale: float, rows=None, nthreads: int = 0):
+    """Branch fusion ("Sparse Attention and Hybrid Attention Architecture
+    Design": out = g * sparse + (1 - g) * local): the token-level layer's
+    pre-gate output and exact attention over positions max(0, t - window + 1)
+    .. t, mixed by g = sigmoid(gate logit)."""
+    L = inp["q"].shape[0]
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    sp = prefill_layer(inp, K, scale, rows=rows, nthreads=nthreads)
+    widx = np.full((len(rows), window), -1, dtype=np.int32)
+    for i, t in enumerate(rows):
+        pos = np.arange(max(0, t - window + 1), t + 1)
+        widx[i, :len(pos)] = pos
+    dv = inp["v"].shape[-1]
+    _, sparse_pre = attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], dv, inp["gate"], rows,
+                           np.zeros_like(rows), sp["idx"], scale, nthreads=nthreads, want_pre=True)
+    _, local_pre = attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], dv, inp["gate"], rows,
+                          np.zeros_like(rows), widx, scale, nthreads=nthreads, want_pre=True)
+    g = 1.0 / (1.0 + np.exp(-inp["gate"].double().numpy()[rows]))[:, :, None]
+    return dict(rows=rows, idx=sp["idx"], out=g * sparse_pre + (1.0 - g) * local_pre)
 
 
 def decode_layer(inp, K: int, dv: int, scale: float, seqs=None, nthreads: int = 0):

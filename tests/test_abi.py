@@ -221,3 +221,15 @@ def test_blocks_workspace(lib):
     n = lib.sa_prefill_blocks_workspace_size(ctypes.byref(a), 16)
     assert n > 0 and n % 256 == 0
     assert lib.sparse_attn_prefill_blocks(ctypes.byref(a), 16, None, 0, None) == binding.SA_ERR_WORKSPACE
+
+
+def test_local_branch_argument_errors(lib):
+    a = _prefill()
+    assert lib.sa_prefill_local_workspace_size(ctypes.byref(a), 0) == 0
+    assert lib.sparse_attn_prefill_local(ctypes.byref(a), 0, None, 0, None) == binding.SA_ERR_INVALID_ARG
+    f = _prefill(attn_dtype=binding.SA_F32)
+    assert lib.sa_prefill_local_workspace_size(ctypes.byref(f), 64) == 0
+    assert lib.sparse_attn_prefill_local(ctypes.byref(f), 64, None, 0, None) == binding.SA_ERR_UNSUPPORTED
+    n = lib.sa_prefill_local_workspace_size(ctypes.byref(a), 64)
+    assert n > lib.sa_prefill_workspace_size(ctypes.byref(a))
+    assert lib.sparse_attn_prefill_local(ctypes.byref(a), 64, None, 0, None) == binding.SA_ERR_WORKSPACE

@@ -487,3 +487,37 @@ def test_blocks_covering_the_history_give_full_causal_attention():
     np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-13)
     for i, t in enumerate(res["rows"]):
         assert res["idx"][i].tolist() == list(range(t + 1)) + [-1] * (cfg.K - t - 1)
+
+
+# ---------------------------------------------------------------------------
+# branch fusion with a sliding-window local branch
+# ---------------------------------------------------------------------------
+
+def test_local_fusion_with_whole_history_is_ungated_causal_attention():
+    from workloads import get_config, make_prefill
+    cfg = get_config("tiny", L=60, K=64, Hq=2)
+    inp = make_prefill(cfg, seed=8)
+    scale = 1 / math.sqrt(cfg.dqk)
+    res = oracle.prefill_local_layer(inp, cfg.K, 64, scale)          # both branches see every position
+    ungated = _torch_gated_causal(inp["q"], inp["k"], inp["v"], torch.full_like(inp["gate"], 60.0), scale).numpy()
+    np.testing.assert_allclose(res["out"], ungated, rtol=1e-12, atol=1e-14)
+
+
+def test_local_fusion_gate_extremes_pick_one_branch():
+    from workloads import get_config, make_prefill
+    cfg = get_config("tiny", L=50, K=8, Hq=2)
+    inp = make_prefill(cfg, seed=9)
+    scale = 1 / math.sqrt(cfg.dqk)
+    L = cfg.L
+    for sign in (1.0, -1.0):
+        inp["gate"] = torch.full((L, cfg.Hq), 60.0 * sign)
+        res = oracle.prefill_local_layer(inp, cfg.K, 5, scale)
+        if sign > 0:                                           # g = 1: the sparse branch, pre-gate
+            sp = oracle.prefill_layer(inp, cfg.K, scale)
+            _, pre = oracle.attend(inp["q"], inp["k"], inp["v"], cfg.dqk, cfg.dv, cfg.dv, inp["gate"], np.arange(L),
+                                   np.zeros(L), sp["idx"], scale, want_pre=True)
+        else:                                                  # g = 0: attention over the last 5 positions
+            widx = np.array([[p if p >= 0 else -1 for p in range(t - 4, t + 1)] for t in range(L)], dtype=np.int32)
+            _, pre = oracle.attend(inp["q"], inp["k"], inp["v"], cfg.dqk, cfg.dv, cfg.dv, inp["gate"], np.arange(L),
+                                   np.zeros(L), widx, scale, want_pre=True)
+        np.testing.assert_allclose(res["out"], pre, rtol=1e-12, atol=1e-14)
