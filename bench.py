@@ -7,7 +7,9 @@ One step = one sparse_attn_decode call for a batch of 32 sequences, each with
 combine. Prints one JSON line (rank 0). Also reports, in the same line, the
 prefill throughput of the 8K and 128K workloads with the tensor-core rate of
 their indexers, the dominant kernel's roofline, an end-to-end number through
-host buffers, and the fp64 oracle timed on the host.
+host buffers, the fp64 oracle timed on the host, and at the 8K prefill shapes
+the gradients over the kept set (fp32 CUDA-core rate), the block-granular
+selection and the local-branch fusion.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -315,6 +317,77 @@ def indexer_roofline(sa, torch, dev, cfg, inp, iters):
             "algorithmic_flops": flops, "ms": ms, "dtype": str(inp["q_idx"].dtype).replace("torch.", "")}
 
 
+FP32_ALU_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12   # SMs x fp32 lanes x FMA x max SM clock
+
+
+def bench_backward(sa, torch, dev, seed, iters=3):
+    """Gradients over the index set the prefill selects, at the 8K prefill
+    shapes: tok/s and the fp32 CUDA-core rate (14 * Hq * d FLOP per kept
+    (query, key) pair: the forward recomputed, then q.k, do.v, dq, dk, dv)."""
+    from workloads import get_config, make_prefill
+    cfg = get_config(PREFILL_WORKLOAD)
+    inp = make_prefill(cfg, seed=seed, device=dev)
+    scale = 1 / math.sqrt(cfg.dqk)
+    idx = torch.empty((cfg.L, cfg.K), dtype=torch.int32, device=dev)
+    sa.sparse_attn_prefill(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], inp["w"], inp["gate"],
+                           cfg.K, scale, idx_out=idx)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 1)
+    dout = torch.randn((cfg.L, cfg.Hq, cfg.dv), generator=g, device=dev).to(cfg.attn_dtype)
+
+    def step():
+        return sa.sparse_attn_backward(inp["q"], inp["k"], inp["v"], idx, inp["gate"], dout, scale)
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    pairs = sum(min(cfg.K, t + 1) for t in range(cfg.L))
+    flops = 14 * cfg.Hq * cfg.dqk * pairs
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": cfg.name, "L": cfg.L, "K": cfg.K, "ms": ms, "tok_s": cfg.L / (ms * 1e-3),
+            "roofline": {"kernel": "attn_bwd_kernel", "bound": "alu", "achieved": tf,
+                         "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_PEAK_TFLOPS,
+                         "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 x 2032 MHz",
+                         "algorithmic_flops": flops}}
+
+
+def bench_variants(sa, torch, dev, seed, iters=5):
+    """The block-granular and the local-branch prefill at the 8K prefill shapes
+    (tok/s; selection and attention split by events for the block variant)."""
+    from workloads import get_config, make_prefill
+    cfg = get_config(PREFILL_WORKLOAD)
+    inp = make_prefill(cfg, seed=seed, device=dev)
+    scale = 1 / math.sqrt(cfg.dqk)
+    out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
+    res = {}
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+    for bs in (64, 16):
+        ms = timed(lambda: sa.sparse_attn_prefill_blocks(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"],
+                                                         inp["w"], inp["gate"], cfg.K, scale, bs, out=out))
+        res[f"blocks_{bs}"] = {"workload": cfg.name, "block_size": bs, "K": cfg.K, "ms": ms,
+                               "tok_s": cfg.L / (ms * 1e-3)}
+    for win in (512,):
+        ms = timed(lambda: sa.sparse_attn_prefill_local(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"],
+                                                        inp["w"], inp["gate"], cfg.K, scale, win, out=out))
+        res[f"local_{win}"] = {"workload": cfg.name, "window": win, "K": cfg.K, "ms": ms, "tok_s": cfg.L / (ms * 1e-3)}
+    return res
+
+
 def bench_prefill(sa, torch, dev, seed, name, iters):
     """Prefill tok/s of one workload (stage split by events), plus the tensor
     rate of its indexer."""
@@ -452,12 +525,14 @@ def run_ours(args):
     e2e = {"value": aggregate_throughput(cfg.B, world, e2e_s), "unit": "tok/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    prefill = None
+    prefill = backward = variants = None
     if not args.no_prefill:
         del host, inp
         torch.cuda.empty_cache()
         prefill = [bench_prefill(sa, torch, dev, args.seed + rank, PREFILL_WORKLOAD, 10),
                    bench_prefill(sa, torch, dev, args.seed + rank, "prefill_128k", 2)]
+        backward = bench_backward(sa, torch, dev, args.seed + rank)
+        variants = bench_variants(sa, torch, dev, args.seed + rank)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -474,7 +549,8 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": workload_config(cfg), "roofline": roofline, "stages_ms": stage,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * K,
-                "clocks": clocks.summary(), "prefill": prefill}
+                "clocks": clocks.summary(), "prefill": prefill, "backward": backward,
+                "variants": variants}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
