@@ -9,7 +9,8 @@ prefill throughput of the 8K and 128K workloads with the tensor-core rate of
 their indexers, the dominant kernel's roofline, an end-to-end number through
 host buffers, the fp64 oracle timed on the host, and at the 8K prefill shapes
 the gradients over the kept set (fp32 CUDA-core rate), the block-granular
-selection and the local-branch fusion.
+selection, the local-branch fusion, and dense causal attention against the
+sparse layer across lengths (the break-even).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -388,6 +389,51 @@ def bench_variants(sa, torch, dev, seed, iters=5):
     return res
 
 
+def bench_break_even(sa, torch, dev, seed, lengths=(4096, 8192, 16384, 32768), iters=3):
+    """Full attention against the sparse layer across lengths, at the 8K
+    prefill's shapes (K = 2048): dense causal attention time, and the sparse
+    prefill split into selection (indexer + Top-K) and sparse attention;
+    saving = full - sparse attention - selection (> 0: the sparse layer wins)."""
+    from workloads import get_config, make_prefill
+    rows = []
+    for L in lengths:
+        cfg = get_config(PREFILL_WORKLOAD, L=L)
+        inp = make_prefill(cfg, seed=seed, device=dev)
+        scale = 1 / math.sqrt(cfg.dqk)
+        out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
+
+        def dense():
+            sa.attention_dense_causal(inp["q"], inp["k"], inp["v"], inp["gate"], scale, out=out)
+
+        def sparse(ev=None):
+            sa.sparse_attn_prefill(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], inp["w"], inp["gate"],
+                                   cfg.K, scale, out=out, stage_events=ev)
+        dense()
+        sparse()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            dense()
+        e1.record()
+        torch.cuda.synchronize()
+        dense_ms = e0.elapsed_time(e1) / iters
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
+        queue_ahead(torch, 0.02)
+        for i in range(iters):
+            ev[i][0].record()
+            sparse(ev[i][1:])
+        torch.cuda.synchronize()
+        sel = statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(iters))
+        att = statistics.median(ev[i][1].elapsed_time(ev[i][2]) for i in range(iters))
+        flops = 4 * cfg.Hq * cfg.dqk * (L * (L + 1) // 2)
+        rows.append({"L": L, "K": cfg.K, "dense_ms": dense_ms, "dense_tflops": flops / (dense_ms * 1e-3) / 1e12,
+                     "selection_ms": sel, "sparse_attention_ms": att, "saving_ms": dense_ms - att - sel})
+        del inp, out
+        torch.cuda.empty_cache()
+    return rows
+
+
 def bench_prefill(sa, torch, dev, seed, name, iters):
     """Prefill tok/s of one workload (stage split by events), plus the tensor
     rate of its indexer."""
@@ -533,6 +579,7 @@ def run_ours(args):
                    bench_prefill(sa, torch, dev, args.seed + rank, "prefill_128k", 2)]
         backward = bench_backward(sa, torch, dev, args.seed + rank)
         variants = bench_variants(sa, torch, dev, args.seed + rank)
+        variants["break_even"] = bench_break_even(sa, torch, dev, args.seed + rank)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -189,6 +189,19 @@ SA_API int sparse_attn_prefill_local(const sa_prefill_args* args, int window, vo
                                      cudaStream_t stream);
 
 /*
+ * Dense causal attention with the sigmoid output gate: query t attends over
+ * every position 0..t (the full-attention layer the sparse one replaces;
+ * "From Full Attention to Sparsity" measures the sparse layer against it:
+ * sparse attention pays off once the indexer costs less than the attention
+ * it saves). q [L, Hq, d], k rows [L, ld_k], v rows [L, ld_v], gate [L, Hq]
+ * logits, out [L, Hq, d]. Supported: bf16, d in {64, 128}, 1 <= Hq <= 64,
+ * ld_k, ld_v multiples of 8, 16-byte aligned q, k, v, out.
+ */
+SA_API int attention_dense_causal(const void* q, const void* k, int64_t ld_k, const void* v, int64_t ld_v,
+                                  const float* gate, void* out, int L, int Hq, int d, float softmax_scale,
+                                  cudaStream_t stream);
+
+/*
  * One decode step for B sequences: the new query of sequence b attends over
  * its ctx_len[b] cached rows, stored at packed rows seq_start[b] ..
  * seq_start[b] + ctx_len[b] - 1 of the caches (append the new token's own

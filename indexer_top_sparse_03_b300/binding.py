@@ -96,6 +96,8 @@ def load_library(path: str | None = None):
     lib.sa_prefill_local_workspace_size.restype = _SZ
     lib.sparse_attn_prefill_local.argtypes = [ctypes.POINTER(PrefillArgs), _I, _P, _SZ, _P]
     lib.sparse_attn_prefill_local.restype = _I
+    lib.attention_dense_causal.argtypes = [_P, _P, _I64, _P, _I64, _P, _P, _I, _I, _I, _F, _P]
+    lib.attention_dense_causal.restype = _I
     lib.sparse_attn_backward.argtypes = [ctypes.POINTER(BackwardArgs), _P]
     lib.sparse_attn_backward.restype = _I
     if path is None:
@@ -281,6 +283,18 @@ def sparse_attn_prefill_local(q, k, v, q_idx, k_idx, w, gate, K: int, softmax_sc
     st = lib.sparse_attn_prefill_local(ctypes.byref(a), window, _ptr(ws), ws.numel() * ws.element_size(),
                                        _stream(q.device, stream))
     _check("sparse_attn_prefill_local", st)
+    return out
+
+
+def attention_dense_causal(q, k, v, gate, softmax_scale: float, out=None, stream=None):
+    """Dense causal gated attention (the full-attention control branch):
+    q [L, Hq, d] bf16, k and v rows [L, ld] bf16, gate [L, Hq]; returns out."""
+    L, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((L, Hq, d), dtype=q.dtype, device=q.device)
+    st = load_library().attention_dense_causal(_ptr(q), _ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(gate),
+                                               _ptr(out), L, Hq, d, softmax_scale, _stream(q.device, stream))
+    _check("attention_dense_causal", st)
     return out
 
 

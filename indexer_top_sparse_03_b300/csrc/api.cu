@@ -601,6 +601,23 @@ int sparse_attn_prefill_local(const sa_prefill_args* args, int window, void* ws,
     return SA_OK;
 }
 
+int attention_dense_causal(const void* q, const void* k, int64_t ld_k, const void* v, int64_t ld_v,
+                           const float* gate, void* out, int L, int Hq, int d, float softmax_scale,
+                           cudaStream_t stream)
+{
+    if (L < 0 || Hq < 1 || d < 1 || ld_k < d || ld_v < d) return SA_ERR_INVALID_ARG;
+    if (!(softmax_scale == softmax_scale)) return SA_ERR_INVALID_ARG;
+    sa::DenseArgs a{};
+    a.q = q; a.k = k; a.ld_k = ld_k; a.v = v; a.ld_v = ld_v; a.gate = gate; a.out = out;
+    a.L = L; a.Hq = Hq; a.D = d; a.softmax_scale = softmax_scale;
+    if (!sa::attention_dense_supported(a)) return SA_ERR_UNSUPPORTED;
+    if (L == 0) return SA_OK;
+    if (!q || !k || !v || !gate || !out) return SA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(gate, 4))
+        return SA_ERR_INVALID_ARG;
+    return status_of(sa::launch_attention_dense(a, stream));
+}
+
 size_t sa_decode_workspace_size(const sa_decode_args* args)
 {
     if (check_decode_scalars(args) != SA_OK) return 0;

@@ -156,6 +156,22 @@ cudaError_t launch_block_rowlen(int64_t t0, int rows, int lg, int32_t* row_len, 
 cudaError_t launch_expand_blocks(const int32_t* blk, int Kb, int64_t t0, int rows, int lg, int32_t* idx,
                                  int32_t* count, cudaStream_t s);
 
+// ---- dense causal attention (the full-attention control branch) ------------
+struct DenseArgs {
+    const void* q;           // [L, Hq, D] bf16
+    const void* k;           // row j at k + j * ld_k
+    int64_t ld_k;
+    const void* v;
+    int64_t ld_v;
+    const float* gate;       // [L, Hq]
+    void* out;               // [L, Hq, D] bf16
+    int64_t L;
+    int Hq, D;
+    float softmax_scale;
+};
+bool attention_dense_supported(const DenseArgs& a);
+cudaError_t launch_attention_dense(const DenseArgs& a, cudaStream_t s);
+
 // ---- sliding-window local branch ---------------------------------------------
 // idx[r] = positions max(0, t - W + 1) .. t (t = t0 + r), ascending, W per row
 // (-1 padded); kept[r] = their count

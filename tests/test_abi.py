@@ -233,3 +233,17 @@ def test_local_branch_argument_errors(lib):
     n = lib.sa_prefill_local_workspace_size(ctypes.byref(a), 64)
     assert n > lib.sa_prefill_workspace_size(ctypes.byref(a))
     assert lib.sparse_attn_prefill_local(ctypes.byref(a), 64, None, 0, None) == binding.SA_ERR_WORKSPACE
+
+
+def test_dense_argument_errors(lib):
+    f = 1 << 20
+    args = lambda **kw: dict(dict(q=f, k=f, ld_k=128, v=f, ld_v=128, gate=f, out=f, L=64, Hq=16, d=128, s=0.1), **kw)
+    call = lambda a: lib.attention_dense_causal(a["q"], a["k"], a["ld_k"], a["v"], a["ld_v"], a["gate"], a["out"],
+                                                a["L"], a["Hq"], a["d"], a["s"], None)
+    assert call(args(Hq=0)) == binding.SA_ERR_INVALID_ARG
+    assert call(args(ld_k=64)) == binding.SA_ERR_INVALID_ARG
+    assert call(args(d=96, ld_k=96, ld_v=96)) == binding.SA_ERR_UNSUPPORTED
+    assert call(args(Hq=65)) == binding.SA_ERR_UNSUPPORTED
+    assert call(args(q=None)) == binding.SA_ERR_INVALID_ARG
+    assert call(args(out=f + 8)) == binding.SA_ERR_INVALID_ARG
+    assert call(args(L=0)) == binding.SA_OK
