@@ -29,7 +29,9 @@ namespace sa {
 namespace {
 
 constexpr int SCAN_THREADS = 256;           // 8 warps
-constexpr int SCAN_CHUNK = 4096;            // keys per CTA
+constexpr int SCAN_CHUNK_MIN = 4096;        // keys per CTA: chosen per call in this range so that
+constexpr int SCAN_CHUNK_MAX = 16384;       // the grid holds about 256 CTAs (fewer, longer streams
+                                            // per SM measured faster than many short ones)
 __host__ __device__ constexpr int scan_unroll(int di) { return di <= 64 ? 4 : (di == 128 ? 2 : 1); }   // 16-key groups in flight per warp
 
 template <int DI, int NTH>
@@ -46,9 +48,9 @@ decode_scan_kernel(DecodeScanArgs a)
     const int g = lane >> 2, t4 = lane & 3;
     int64_t n = a.ctx_len[b];
     n = n < 0 ? 0 : (n > a.max_ctx ? a.max_ctx : n);
-    const int64_t j0 = (int64_t)blockIdx.x * SCAN_CHUNK;
+    const int64_t j0 = (int64_t)blockIdx.x * a.chunk;
     if (j0 >= n) return;
-    const int cnt = (int)min64(SCAN_CHUNK, n - j0);
+    const int cnt = (int)min64(a.chunk, n - j0);
     __shared__ unsigned sh_hist[HBINS];
     for (int i = tid; i < HBINS; i += SCAN_THREADS) sh_hist[i] = 0;
     __syncthreads();
@@ -144,7 +146,7 @@ decode_scan_kernel(DecodeScanArgs a)
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const unsigned ctas = (unsigned)((n + SCAN_CHUNK - 1) / SCAN_CHUNK);
+        const unsigned ctas = (unsigned)((n + a.chunk - 1) / a.chunk);
         sh_last = atomicAdd(a.row_tickets + b, 1u) == ctas - 1u;
     }
     __syncthreads();
@@ -166,7 +168,7 @@ zero_kernel(uint4* p, size_t n16)
 template <int DI>
 cudaError_t launch_di(const DecodeScanArgs& a, cudaStream_t s)
 {
-    dim3 grid((unsigned)((a.max_ctx + SCAN_CHUNK - 1) / SCAN_CHUNK), a.B);
+    dim3 grid((unsigned)((a.max_ctx + a.chunk - 1) / a.chunk), a.B);
     if (a.Hi <= 8) return launch_kernel(decode_scan_kernel<DI, 1>, grid, dim3(SCAN_THREADS), 0, s, true, a);
     if (a.Hi <= 16) return launch_kernel(decode_scan_kernel<DI, 2>, grid, dim3(SCAN_THREADS), 0, s, true, a);
     return launch_kernel(decode_scan_kernel<DI, 4>, grid, dim3(SCAN_THREADS), 0, s, true, a);
@@ -183,9 +185,13 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_scan(const DecodeScanArgs& a, cudaStream_t s)
+cudaError_t launch_decode_scan(const DecodeScanArgs& args, cudaStream_t s)
 {
-    if (a.B <= 0 || a.max_ctx <= 0) return cudaSuccess;
+    if (args.B <= 0 || args.max_ctx <= 0) return cudaSuccess;
+    DecodeScanArgs a = args;
+    const int64_t keys = (int64_t)a.B * a.max_ctx;
+    a.chunk = SCAN_CHUNK_MIN;
+    while (a.chunk < SCAN_CHUNK_MAX && (int64_t)a.chunk * 256 < keys) a.chunk *= 2;
     switch (a.di) {
     case 32: return launch_di<32>(a, s);
     case 64: return launch_di<64>(a, s);

@@ -269,6 +269,7 @@ struct DecodeScanArgs {
     unsigned* row_tickets;  // [B], zero on entry
     int K;
     BinSplit* split;        // [B] bin of the K-th best score (rows with n > K)
+    int chunk;              // keys per CTA (set by the launcher)
 };
 cudaError_t launch_decode_scan(const DecodeScanArgs& a, cudaStream_t s);
 
