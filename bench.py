@@ -323,8 +323,9 @@ FP32_ALU_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12   # SMs x fp32 lanes x FMA
 
 def bench_backward(sa, torch, dev, seed, iters=3):
     """Gradients over the index set the prefill selects, at the 8K prefill
-    shapes: tok/s and the fp32 CUDA-core rate (14 * Hq * d FLOP per kept
-    (query, key) pair: the forward recomputed, then q.k, do.v, dq, dk, dv)."""
+    shapes: tok/s and the rate of 14 * Hq * d FLOP per kept (query, key) pair
+    (the forward recomputed, then q.k, do.v, dq, dk, dv) against the bf16
+    tensor peak (and, for reference, the fp32 CUDA-core peak)."""
     from workloads import get_config, make_prefill
     cfg = get_config(PREFILL_WORKLOAD)
     inp = make_prefill(cfg, seed=seed, device=dev)
@@ -350,11 +351,13 @@ def bench_backward(sa, torch, dev, seed, iters=3):
     pairs = sum(min(cfg.K, t + 1) for t in range(cfg.L))
     flops = 14 * cfg.Hq * cfg.dqk * pairs
     tf = flops / (ms * 1e-3) / 1e12
+    peaks = measured_peaks()
     return {"workload": cfg.name, "L": cfg.L, "K": cfg.K, "ms": ms, "tok_s": cfg.L / (ms * 1e-3),
-            "roofline": {"kernel": "attn_bwd_kernel", "bound": "alu", "achieved": tf,
-                         "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_PEAK_TFLOPS,
-                         "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 x 2032 MHz",
-                         "algorithmic_flops": flops}}
+            "roofline": {"kernel": "attn_bwd_tc_kernel", "bound": "tensor", "achieved": tf,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                         "peak_source": peaks["source"] + " burst bf16",
+                         "algorithmic_flops": flops,
+                         "fp32_alu_frac": tf / FP32_ALU_PEAK_TFLOPS}}
 
 
 def bench_variants(sa, torch, dev, seed, iters=5):

@@ -315,6 +315,7 @@ cudaError_t launch_attention_backward(const BwdArgs& a, cudaStream_t s)
     cudaError_t e = launch_zero(a.dk, sizeof(float) * (size_t)a.L * a.D, s);
     if (e == cudaSuccess) e = launch_zero(a.dv, sizeof(float) * (size_t)a.L * a.D, s);
     if (e != cudaSuccess) return e;
+    if (attention_backward_tc_supported(a)) return launch_attention_backward_tc(a, s);
     if (a.dtype == SA_BF16) return a.D == 64 ? launch_bwd_t<64, bf16>(a, s) : launch_bwd_t<128, bf16>(a, s);
     return a.D == 64 ? launch_bwd_t<64, float>(a, s) : launch_bwd_t<128, float>(a, s);
 }

@@ -199,7 +199,9 @@ struct BwdArgs {
     float* dgate;            // [L, Hq]
 };
 bool attention_backward_supported(const BwdArgs& a);
-cudaError_t launch_attention_backward(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_attention_backward(const BwdArgs& a, cudaStream_t s);      // picks one of:
+bool attention_backward_tc_supported(const BwdArgs& a);                        // bf16, tensor cores
+cudaError_t launch_attention_backward_tc(const BwdArgs& a, cudaStream_t s);   // (dk, dv zeroed by the caller)
 
 // ---- step 2: Top-K over score rows -----------------------------------------
 struct TopkArgs {
