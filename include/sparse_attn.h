@@ -75,6 +75,16 @@ SA_API const char* sa_status_string(int status);
 SA_API int sa_version(void);
 
 /*
+ * Device-side error bits of the current GPU, ORed since the last reset:
+ * SA_DEVERR_WAIT_TIMEOUT = a bounded wait of the tensor-core indexer gave up
+ * (its outputs are then incomplete; the kernel returned instead of hanging).
+ * Synchronises the device. *bits receives the word; reset != 0 clears it.
+ * Returns SA_OK or SA_ERR_LAUNCH (the copy failed).
+ */
+#define SA_DEVERR_WAIT_TIMEOUT 1u
+SA_API int sa_device_errors(unsigned* bits, int reset);
+
+/*
  * indexer_score -- step 1 alone (exposed for testing).
  *
  *   q_idx   [T, Hi, di]  query-side indexer vectors, dtype `dtype`

@@ -74,6 +74,8 @@ def load_library(path: str | None = None):
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_version.argtypes = []
     lib.sa_version.restype = _I
+    lib.sa_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), _I]
+    lib.sa_device_errors.restype = _I
     lib.indexer_score.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P, _I64, _P]
     lib.indexer_score.restype = _I
     lib.topk_select.argtypes = [_P, _I64, _P, _I, _I, _P, _P]
@@ -103,6 +105,13 @@ def load_library(path: str | None = None):
     if path is None:
         _lib = lib
     return lib
+
+
+def device_errors(reset: bool = False) -> int:
+    """The device-side error bits (SA_DEVERR_*) of the current GPU; synchronises."""
+    bits = ctypes.c_uint(0)
+    _check("sa_device_errors", load_library().sa_device_errors(ctypes.byref(bits), 1 if reset else 0))
+    return bits.value
 
 
 def status_string(status: int) -> str:

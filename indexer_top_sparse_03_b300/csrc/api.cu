@@ -5,6 +5,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.h"
 #include "../../include/sparse_attn.h"
 
@@ -15,6 +17,14 @@ bool attention_mma_supported(const AttnArgs& a);
 namespace {
 
 constexpr size_t WS_ALIGN = 256;
+
+// NVTX range over one entry point or stage (free when no tool is attached)
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 constexpr int MAX_K = 65536;
 
 size_t align_up(size_t x) { return (x + WS_ALIGN - 1) / WS_ALIGN * WS_ALIGN; }
@@ -342,6 +352,12 @@ const char* sa_status_string(int status)
 
 int sa_version(void) { return 100; }
 
+int sa_device_errors(unsigned* bits, int reset)
+{
+    if (!bits) return SA_ERR_INVALID_ARG;
+    return sa::indexer_device_errors(bits, reset != 0) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
 int indexer_score(const void* q_idx, int dtype, const float* q_scale, const float* w,
                   const void* k_idx, const float* k_scale, int T, int N, int Hi, int di,
                   int64_t causal_offset, float* scores, int64_t ld_s, cudaStream_t stream)
@@ -384,6 +400,7 @@ size_t sa_prefill_workspace_size(const sa_prefill_args* args)
 
 int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
+    NvtxRange range("sparse_attn_prefill");
     int st = check_prefill(args);
     if (st != SA_OK) return st;
     const sa_prefill_args& a = *args;
@@ -473,6 +490,7 @@ int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, 
 
 int sparse_attn_backward(const sa_backward_args* args, cudaStream_t stream)
 {
+    NvtxRange range("sparse_attn_backward");
     if (!args) return SA_ERR_INVALID_ARG;
     const sa_backward_args& a = *args;
     if (a.L < 0 || a.Hq < 1 || a.dqk < 1 || a.dv < 1 || a.K < 1) return SA_ERR_INVALID_ARG;
@@ -504,6 +522,7 @@ size_t sa_prefill_blocks_workspace_size(const sa_prefill_args* args, int block_s
 int sparse_attn_prefill_blocks(const sa_prefill_args* args, int block_size, void* ws, size_t ws_bytes,
                                cudaStream_t stream)
 {
+    NvtxRange range("sparse_attn_prefill_blocks");
     int st = check_blocks(args, block_size, false);
     if (st != SA_OK) return st;
     const sa_prefill_args& a = *args;
@@ -565,6 +584,7 @@ size_t sa_prefill_local_workspace_size(const sa_prefill_args* args, int window)
 int sparse_attn_prefill_local(const sa_prefill_args* args, int window, void* ws, size_t ws_bytes,
                               cudaStream_t stream)
 {
+    NvtxRange range("sparse_attn_prefill_local");
     int st = check_prefill(args);
     if (st != SA_OK) return st;
     if (window < 1) return SA_ERR_INVALID_ARG;
@@ -626,6 +646,7 @@ size_t sa_decode_workspace_size(const sa_decode_args* args)
 
 int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
+    NvtxRange range("sparse_attn_decode");
     int st = check_decode(args);
     if (st != SA_OK) return st;
     const sa_decode_args& a = *args;

@@ -642,6 +642,17 @@ int indexer_filter_lcap(const IndexerArgs& a)
 
 int indexer_query_tile(const IndexerArgs& a) { return a.Hi > 0 ? TC_BN / a.Hi : 0; }
 
+cudaError_t indexer_device_errors(unsigned* bits, bool reset)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(bits, g_tc_error, sizeof(unsigned));
+    if (e == cudaSuccess && reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(unsigned));
+    }
+    return e;
+}
+
 bool indexer_tc_supported(const IndexerArgs& a)
 {
     const bool hi_ok = a.Hi == 1 || a.Hi == 2 || a.Hi == 4 || a.Hi == 8 || a.Hi == 16 || a.Hi == 32;

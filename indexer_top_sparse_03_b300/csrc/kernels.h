@@ -111,6 +111,7 @@ cudaError_t launch_indexer_simt(const IndexerArgs& a, cudaStream_t s);   // any 
 cudaError_t launch_indexer_tc(const IndexerArgs& a, cudaStream_t s);     // bf16 / FP8, tensor cores
 bool indexer_tc_supported(const IndexerArgs& a);
 
+cudaError_t indexer_device_errors(unsigned* bits, bool reset);   // the tensor-core indexer's error word
 int indexer_filter_lcap(const IndexerArgs& a);   // pairs per query and work item in filter mode; 0: none
 int indexer_query_tile(const IndexerArgs& a);    // queries per tensor-core tile (256 / Hi)
 constexpr int INDEXER_GROUP = 8;                 // key tiles (of 128) per tensor-core work item

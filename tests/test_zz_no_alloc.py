@@ -80,3 +80,10 @@ def test_noalloc_rejects_requests_beyond_its_scratch(cuda_ok):
     assert lib.sparse_attn_decode_noalloc(ctypes.byref(a), stream) == binding.SA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.isnan(out.float()).all() and (idx.cpu() == -7).all()    # nothing was enqueued
+
+
+def test_no_device_error_bits_after_the_gpu_tests(cuda_ok):
+    # every bounded wait of the tensor-core indexer completed in the runs above
+    import indexer_top_sparse_03_b300 as pkg
+    pkg.load_library()
+    assert pkg.device_errors() == 0
