@@ -360,6 +360,52 @@ def bench_backward(sa, torch, dev, seed, iters=3):
                          "fp32_alu_frac": tf / FP32_ALU_PEAK_TFLOPS}}
 
 
+def bench_decode_config(sa, torch, dev, seed, name, iters=200):
+    """Decode throughput of another decode workload (graph replay of one step)
+    and its whole-step fraction of the HBM roofline (the same byte count as the
+    headline workload: indexer keys scanned + kept rows + small tensors)."""
+    from workloads import get_config, make_decode
+    cfg = get_config(name)
+    inp = make_decode(cfg, seed=seed, device=dev)
+    lens = inp["lens"]
+    scale = 1 / math.sqrt(cfg.dqk)
+    out = torch.empty((cfg.B, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=dev)
+
+    def step():
+        sa.sparse_attn_decode(inp["q"], inp["q_idx"], inp["w"], inp["gate"], inp["k_cache"], inp["v_cache"],
+                              inp["k_idx_cache"], inp["seq_start"], inp["ctx_len"], max(lens), cfg.K, scale,
+                              dv=cfg.dv, ld_k=inp["ld_k"], ld_v=inp["ld_v"], out=out, idx_out=idx)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    step_bytes, _ = decode_bytes(cfg, lens)
+    peak = measured_peaks()["hbm_gbs"]
+    res = {"workload": cfg.name, "B": cfg.B, "ctx_sum": int(sum(lens)), "ms": ms, "tok_s": cfg.B / (ms * 1e-3),
+           "step_bytes": step_bytes, "hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / peak}
+    del graph, inp
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_variants(sa, torch, dev, seed, iters=5):
     """The block-granular and the local-branch prefill at the 8K prefill shapes
     (tok/s; selection and attention split by events for the block variant)."""
@@ -595,13 +641,15 @@ def run_ours(args):
     e2e = {"value": aggregate_throughput(cfg.B, world, e2e_s), "unit": "tok/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    prefill = backward = variants = None
+    prefill = backward = variants = other_decode = None
     if not args.no_prefill:
         del host, inp
         torch.cuda.empty_cache()
         prefill = [bench_prefill(sa, torch, dev, args.seed + rank, PREFILL_WORKLOAD, 10),
                    bench_prefill(sa, torch, dev, args.seed + rank, "prefill_128k", 2)]
         backward = bench_backward(sa, torch, dev, args.seed + rank)
+        other_decode = [bench_decode_config(sa, torch, dev, args.seed + rank, n)
+                        for n in ("decode_mla", "decode_ragged")]
         variants = bench_variants(sa, torch, dev, args.seed + rank)
         variants["break_even"] = bench_break_even(sa, torch, dev, args.seed + rank)
 
@@ -622,7 +670,7 @@ def run_ours(args):
                 "stages_ms": stage,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * K,
                 "clocks": clocks.summary(), "prefill": prefill, "backward": backward,
-                "variants": variants}
+                "variants": variants, "decode_other": other_decode}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -222,7 +222,10 @@ struct DecodeLayout {
 DecodeLayout decode_layout(const sa_decode_args& a)
 {
     DecodeLayout l{};
-    l.splits = sa::attention_splits(a.K, a.max_ctx, a.B);
+    // the self-gathering kernel takes bf16 rows of 64 or 128 with separate values
+    const bool gather = a.attn_dtype == SA_BF16 && a.dqk == a.dv && (a.dqk == 64 || a.dqk == 128) &&
+                        !(a.v_cache == a.k_cache && a.ld_v == a.ld_k);
+    l.splits = sa::attention_splits(a.K, a.max_ctx, a.B, gather);
     const size_t B = (size_t)a.B;
     const int64_t ctx = a.max_ctx > 0 ? a.max_ctx : 1;
     l.ld_w = (ctx + 127) / 128 * 4;             // bitmap words per row, a multiple of 4

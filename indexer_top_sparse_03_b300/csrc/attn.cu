@@ -352,11 +352,14 @@ size_t mma_smem_bytes(const AttnArgs& a, int stages)
 
 constexpr size_t MMA_SMEM_LIMIT = 200 * 1024;    // leaves room for static shared memory
 
-// Pipeline depth: double buffering (the kernel supports up to 4 buffers).
+// Pipeline depth: double buffering (the kernel supports up to 4 buffers)
+// unless that leaves room for only one CTA per SM.
 int attention_stages(const AttnArgs& a)
 {
     // measured: more CTAs per SM beat a deeper pipeline in one CTA
-    return mma_smem_bytes(a, 2) <= MMA_SMEM_LIMIT ? 2 : 1;
+    // (the 576-wide latent row: 2 stages, one CTA per SM, 241 us per decode
+    // step at 64 x 32K; 1 stage, two CTAs per SM, 203 us)
+    return mma_smem_bytes(a, 2) <= 110 * 1024 ? 2 : 1;
 }
 
 template <int NT>
@@ -385,16 +388,20 @@ bool attention_mma_supported(const AttnArgs& a)
     return true;
 }
 
-// Splits of the kept rows per query row for the decode attention: enough CTAs
-// for about two waves on 148 SMs, at least 256 kept rows per CTA.
-int attention_splits(int K, int64_t n_cap, int rows)
+// Splits of the kept rows per query row for the decode attention. The
+// self-gathering kernel: about two waves of CTAs on 148 SMs, at least 256
+// kept rows per CTA. The shared-tile kernel (wide latent rows, one CTA per SM
+// at most two): about four waves, at least 128 kept rows per CTA. Both
+// measured against more and fewer splits.
+int attention_splits(int K, int64_t n_cap, int rows, bool gather_kernel)
 {
     const int64_t kept = min64(K, n_cap);
-    const int target = 2 * 148;
-    if (kept <= 256 || rows <= 0 || rows >= target) return 1;
+    const int target = (gather_kernel ? 2 : 4) * 148;
+    const int64_t min_per = gather_kernel ? 256 : 128;
+    if (kept <= min_per || rows <= 0 || rows >= target) return 1;
     const int want = (target + rows - 1) / rows;
     int64_t per = (kept + want - 1) / want;
-    per = max64(max64(256, (K + MAX_SPLITS - 1) / MAX_SPLITS), per);
+    per = max64(max64(min_per, (K + MAX_SPLITS - 1) / MAX_SPLITS), per);
     per = (per + CHUNK - 1) / CHUNK * CHUNK;
     return (int)((K + per - 1) / per);
 }

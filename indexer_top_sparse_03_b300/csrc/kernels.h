@@ -247,7 +247,7 @@ struct AttnArgs {
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);          // picks one of:
 bool attention_gather_supported(const AttnArgs& a);                       // TMA gather4, dv <= 128
 cudaError_t launch_attention_gather(const AttnArgs& a, cudaStream_t s);
-int attention_splits(int K, int64_t n_cap, int rows);
+int attention_splits(int K, int64_t n_cap, int rows, bool gather_kernel);
 
 // Bin of the K-th best score of a row, from a 4096-bin histogram of the top
 // 12 bits of the scores' order-preserving keys.
