@@ -272,7 +272,8 @@ struct DecodeScanArgs {
     unsigned* row_tickets;  // [B], zero on entry
     int K;
     BinSplit* split;        // [B] bin of the K-th best score (rows with n > K)
-    int chunk;              // keys per CTA (set by the launcher)
+    int chunk;              // keys per chunk (set by the launcher)
+    int b_begin, nb;        // rows of one launch (set by the launcher)
 };
 cudaError_t launch_decode_scan(const DecodeScanArgs& a, cudaStream_t s);
 
