@@ -431,7 +431,7 @@ int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, 
             if (e != cudaSuccess) return SA_ERR_LAUNCH;
             sa::TopkArgs ta{};
             ta.scores = scores; ta.ld_s = lay.ld_s; ta.row_len = nullptr; ta.causal_first = t0;
-            ta.n_cap = a.L; ta.rows = (int)(t1 - t0); ta.K = a.K; ta.idx = idx + t0 * a.K; ta.ld_idx = a.K;
+            ta.n_cap = t1; ta.rows = (int)(t1 - t0); ta.K = a.K; ta.idx = idx + t0 * a.K; ta.ld_idx = a.K;
             e = sa::launch_topk(ta, stream);
             if (e != cudaSuccess) return SA_ERR_LAUNCH;
         } else {

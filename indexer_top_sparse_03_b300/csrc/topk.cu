@@ -217,11 +217,61 @@ topk_rows_kernel(TopkArgs a)
     }
 }
 
+// Rows that all fit the stage (n_cap <= STAGE_MAX): small CTAs, so that many
+// rows are in flight per SM (one row's radix passes are short and end in
+// block barriers), and shared memory sized to the longest row.
+template <int NT>
+__global__ void __launch_bounds__(NT)
+topk_short_kernel(TopkArgs a)
+{
+    __shared__ RadixShared sh;
+    extern __shared__ __align__(16) unsigned char tk_smem[];
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int64_t n = topk_row_len(a, r);
+    const int K = a.K;
+    int32_t* out = a.idx + (int64_t)r * a.ld_idx;
+    const float* row = a.scores + (int64_t)r * a.ld_s;
+    if (n <= K) {
+        for (int i = tid; i < K; i += NT) out[i] = i < n ? i : -1;
+        return;
+    }
+    uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem);
+    int64_t j_tail = 0;
+    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+        const int64_t n4 = n / 4;
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+        uint4* k4 = reinterpret_cast<uint4*>(keys);
+#pragma unroll 4
+        for (int64_t i = tid; i < n4; i += NT) {
+            const float4 v = __ldcs(r4 + i);
+            k4[i] = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+        }
+        j_tail = n4 * 4;
+    }
+    for (int64_t j = j_tail + tid; j < n; j += NT) keys[j] = score_key(__ldcs(row + j));
+    __syncthreads();
+    radix_select_row([&](int64_t j) { return keys[j]; }, n, K, out, sh);
+}
+
+constexpr int TK_SHORT_THREADS = 128;
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s)
 {
     if (a.rows <= 0) return cudaSuccess;
+    if (a.n_cap > a.K && a.n_cap <= STAGE_MAX) {
+        const size_t ssm = ((size_t)a.n_cap * 4 + 15) / 16 * 16;
+        cudaError_t e = cudaFuncSetAttribute(topk_short_kernel<TK_SHORT_THREADS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e;
+        }
+        topk_short_kernel<TK_SHORT_THREADS><<<a.rows, TK_SHORT_THREADS, ssm, s>>>(a);
+        return cudaGetLastError();
+    }
     const size_t smem = a.n_cap <= a.K ? 0 : TK_SMEM;
     if (smem) {
         cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

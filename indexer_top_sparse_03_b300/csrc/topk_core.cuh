@@ -262,33 +262,53 @@ __device__ void radix_select_row(KeyAt key_at, int64_t n, int K, int32_t* out, R
     }
 
     // ordered emission: keys above the threshold, plus the first `need`
-    // (lowest positions) of those equal to it
+    // (lowest positions) of those equal to it. Each warp takes 32 x EMIT_STEPS
+    // consecutive positions per round (32 per step, one ballot pair per step),
+    // so a round of the block covers nth x EMIT_STEPS positions with one
+    // exchange of warp totals.
+    constexpr int EMIT_STEPS = 8;
     const uint32_t lanemask_lt = (1u << lane) - 1u;
+    const int nw = nth >> 5;
     unsigned written = 0, eq_before = 0;
-    for (int64_t j0 = 0; j0 < n; j0 += nth) {
-        const int64_t j = j0 + tid;
-        bool gt = false, eq = false;
-        if (j < n) {
-            const uint32_t u = key_at(j) & mask;
-            gt = u > prefix;
-            eq = u == prefix;
+    for (int64_t j0 = 0; j0 < n; j0 += (int64_t)nth * EMIT_STEPS) {
+        const int64_t wb = j0 + (int64_t)warp * 32 * EMIT_STEPS;
+        unsigned bgt[EMIT_STEPS], beq[EMIT_STEPS];
+        unsigned cgt = 0, ceq = 0;
+#pragma unroll
+        for (int i = 0; i < EMIT_STEPS; ++i) {
+            const int64_t j = wb + i * 32 + lane;
+            bool gt = false, eq = false;
+            if (j < n) {
+                const uint32_t u = key_at(j) & mask;
+                gt = u > prefix;
+                eq = u == prefix;
+            }
+            bgt[i] = __ballot_sync(0xffffffffu, gt);
+            beq[i] = __ballot_sync(0xffffffffu, eq);
+            cgt += __popc(bgt[i]);
+            ceq += __popc(beq[i]);
         }
-        const unsigned bgt = __ballot_sync(0xffffffffu, gt);
-        const unsigned beq = __ballot_sync(0xffffffffu, eq);
-        if (lane == 0) sh.warp_tot[warp] = __popc(bgt) | (__popc(beq) << 16);
+        if (lane == 0) sh.warp_tot[warp] = cgt | (ceq << 16);
         __syncthreads();
         unsigned wpre = 0, tot = 0;
-        for (int w = 0; w < (nth >> 5); ++w) {
+        for (int w = 0; w < nw; ++w) {
             const unsigned v = sh.warp_tot[w];
             wpre += (w < warp) ? v : 0u;
             tot += v;
         }
-        const unsigned gt_ex = (wpre & 0xffff) + __popc(bgt & lanemask_lt);
-        const unsigned eq_ex = (wpre >> 16) + __popc(beq & lanemask_lt);
         const unsigned eq_quota = need > eq_before ? need - eq_before : 0u;
-        if (gt || (eq && eq_ex < eq_quota)) {
-            const unsigned pos = written + gt_ex + min(eq_ex, eq_quota);
-            if (pos < (unsigned)K) out[pos] = (int32_t)j;
+        unsigned gt_run = wpre & 0xffff, eq_run = wpre >> 16;
+#pragma unroll
+        for (int i = 0; i < EMIT_STEPS; ++i) {
+            const unsigned gt_ex = gt_run + __popc(bgt[i] & lanemask_lt);
+            const unsigned eq_ex = eq_run + __popc(beq[i] & lanemask_lt);
+            const bool gt = (bgt[i] >> lane) & 1u, eq = (beq[i] >> lane) & 1u;
+            if (gt || (eq && eq_ex < eq_quota)) {
+                const unsigned pos = written + gt_ex + min(eq_ex, eq_quota);
+                if (pos < (unsigned)K) out[pos] = (int32_t)(wb + i * 32 + lane);
+            }
+            gt_run += __popc(bgt[i]);
+            eq_run += __popc(beq[i]);
         }
         written += (tot & 0xffff) + min(tot >> 16, eq_quota);
         eq_before += tot >> 16;
