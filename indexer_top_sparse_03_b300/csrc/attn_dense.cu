@@ -12,6 +12,13 @@
 // Q K^T, an fp32 online softmax in the exp2 domain, O += P V, and at the end
 // the gate and a bf16 store of its own row. CTAs are issued from the last
 // query rows down, so that the longest rows start first.
+//
+// With a kept-position list (rows t >= mask_from), each such warp first sets
+// one bit per kept position of its query in a shared-memory bitmap; the
+// logits of the other positions are -inf and 16-row steps without a kept
+// position are skipped. That is exact attention over the kept set, and it is
+// cheaper than gathering the rows one query at a time while the kept set is
+// a large share of the history.
 #include "attn_common.cuh"
 #include "../../include/sparse_attn.h"
 
@@ -29,8 +36,10 @@ struct DnCfg {
     static constexpr int TBYTES = DN_TILE * LDP * 2;            // one K (or V) tile
     static constexpr int STAGE = 2 * TBYTES;                    // K and V
     static constexpr int QBYTES = 16 * LDP * 2;                 // one warp's Q tile
-    static constexpr int SMEM = DN_STAGES * STAGE + DN_W * QBYTES;
+    static constexpr int SMEM = DN_STAGES * STAGE + DN_W * QBYTES;    // + DN_W bitmaps when masked
 };
+
+__host__ __device__ __forceinline__ int64_t dense_mask_words(const DenseArgs& a) { return a.idx ? (a.L + 31) / 32 : 0; }
 
 template <int D>
 __global__ void __launch_bounds__(DN_THREADS, 2)
@@ -86,6 +95,21 @@ attn_dense_kernel(DenseArgs a)
     const float sl2 = a.softmax_scale * LOG2E;
     const uint32_t qbase = smem_u32(Qs + warp * 16 * C::LDP);
 
+    // kept-position bitmap of this warp's query (rows t >= mask_from)
+    const bool masked = a.idx != nullptr && t >= a.mask_from && t < a.L;
+    uint32_t* bm = reinterpret_cast<uint32_t*>(dn_smem + C::SMEM) + warp * dense_mask_words(a);
+    if (masked) {
+        const int words = (int)(t >> 5) + 1;
+        for (int i = lane; i < words; i += 32) bm[i] = 0u;
+        __syncwarp();
+        const int32_t* sel = a.idx + t * a.K;
+        for (int i = lane; i < a.K; i += 32) {
+            const int32_t p = sel[i];
+            if (p >= 0 && p <= t) atomicOr(&bm[p >> 5], 1u << (p & 31));
+        }
+        __syncwarp();
+    }
+
     issue(0);
     for (int kt = 0; kt < ntiles; ++kt) {
         issue(kt + 1);
@@ -96,6 +120,11 @@ attn_dense_kernel(DenseArgs a)
         for (int s16 = 0; s16 < DN_TILE / 16; ++s16) {
             const int64_t j0 = (int64_t)kt * DN_TILE + s16 * 16;
             if (j0 > t) break;                                    // warp-uniform: past this query
+            uint32_t keep = 0xFFFFu;                              // kept rows of this step (bit i: j0 + i)
+            if (masked) {
+                keep = (bm[j0 >> 5] >> (j0 & 31)) & 0xFFFFu;
+                if (keep == 0u) continue;                         // warp-uniform: nothing kept here
+            }
             float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -112,7 +141,8 @@ attn_dense_kernel(DenseArgs a)
             for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool valid = j0 + nt * 8 + 2 * t4 + e <= t;
+                    const int c = nt * 8 + 2 * t4 + e;
+                    const bool valid = j0 + c <= t && ((keep >> c) & 1u);
                     sc[nt][e] = valid ? sc[nt][e] * sl2 : -INFINITY;
                     sc[nt][2 + e] = valid ? sc[nt][2 + e] * sl2 : -INFINITY;
                     mx0 = fmaxf(mx0, sc[nt][e]);
@@ -179,10 +209,11 @@ attn_dense_kernel(DenseArgs a)
 template <int D>
 cudaError_t launch_dense_d(const DenseArgs& a, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(attn_dense_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DnCfg<D>::SMEM);
+    const size_t smem = DnCfg<D>::SMEM + (size_t)DN_W * dense_mask_words(a) * 4;
+    cudaError_t e = cudaFuncSetAttribute(attn_dense_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.L + DN_W - 1) / DN_W), 1, (unsigned)((a.Hq + 15) / 16));
-    attn_dense_kernel<D><<<grid, DN_THREADS, DnCfg<D>::SMEM, s>>>(a);
+    attn_dense_kernel<D><<<grid, DN_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -190,7 +221,10 @@ cudaError_t launch_dense_d(const DenseArgs& a, cudaStream_t s)
 
 bool attention_dense_supported(const DenseArgs& a)
 {
-    return (a.D == 64 || a.D == 128) && a.Hq >= 1 && a.Hq <= 64 && a.ld_k % 8 == 0 && a.ld_v % 8 == 0;
+    const int64_t mask_bytes = (int64_t)DN_W * dense_mask_words(a) * 4;
+    const int64_t base = a.D == 64 ? DnCfg<64>::SMEM : DnCfg<128>::SMEM;
+    return (a.D == 64 || a.D == 128) && a.Hq >= 1 && a.Hq <= 64 && a.ld_k % 8 == 0 && a.ld_v % 8 == 0 &&
+           (!a.idx || (a.K >= 1 && base + mask_bytes <= 200 * 1024));
 }
 
 cudaError_t launch_attention_dense(const DenseArgs& a, cudaStream_t s)

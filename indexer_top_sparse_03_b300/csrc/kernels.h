@@ -169,6 +169,11 @@ struct DenseArgs {
     int64_t L;
     int Hq, D;
     float softmax_scale;
+    // optional kept-position mask: rows t >= mask_from attend only to the
+    // positions listed in idx[t * K .. t * K + K) (all <= t); null = dense
+    const int32_t* idx;
+    int K;
+    int64_t mask_from;
 };
 bool attention_dense_supported(const DenseArgs& a);
 cudaError_t launch_attention_dense(const DenseArgs& a, cudaStream_t s);

@@ -236,7 +236,11 @@ topk_short_kernel(TopkArgs a)
         for (int i = tid; i < K; i += NT) out[i] = i < n ? i : -1;
         return;
     }
+    // stage the row's keys and count their top digits (the radix select's
+    // first pass) on the way
     uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem);
+    for (int i = tid; i < RADIX; i += NT) sh.hist[i] = 0;
+    __syncthreads();
     int64_t j_tail = 0;
     if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
         const int64_t n4 = n / 4;
@@ -245,13 +249,20 @@ topk_short_kernel(TopkArgs a)
 #pragma unroll 4
         for (int64_t i = tid; i < n4; i += NT) {
             const float4 v = __ldcs(r4 + i);
-            k4[i] = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+            const uint4 k = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+            k4[i] = k;
+            atomicAdd(&sh.hist[k.x >> 24], 1u); atomicAdd(&sh.hist[k.y >> 24], 1u);
+            atomicAdd(&sh.hist[k.z >> 24], 1u); atomicAdd(&sh.hist[k.w >> 24], 1u);
         }
         j_tail = n4 * 4;
     }
-    for (int64_t j = j_tail + tid; j < n; j += NT) keys[j] = score_key(__ldcs(row + j));
+    for (int64_t j = j_tail + tid; j < n; j += NT) {
+        const uint32_t k = score_key(__ldcs(row + j));
+        keys[j] = k;
+        atomicAdd(&sh.hist[k >> 24], 1u);
+    }
     __syncthreads();
-    radix_select_row([&](int64_t j) { return keys[j]; }, n, K, out, sh);
+    radix_select_row<true>([&](int64_t j) { return keys[j]; }, n, K, out, sh);
 }
 
 constexpr int TK_SHORT_THREADS = 128;

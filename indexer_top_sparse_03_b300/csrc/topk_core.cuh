@@ -237,20 +237,24 @@ SA_DEVINL uint32_t block_max_u32(uint32_t v, unsigned* warp_tot)
 // Keeps the K best of the n keys given by key_at(j) (n > K) and writes their
 // positions in ascending order to out[0 .. K-1]. Whole block, blockDim.x a
 // multiple of 32.
-template <typename KeyAt>
+// With HIST0 the caller has already counted the top digits (key >> 24) of
+// all n keys into sh.hist (and synchronised), so the first pass is skipped.
+template <bool HIST0 = false, typename KeyAt>
 __device__ void radix_select_row(KeyAt key_at, int64_t n, int K, int32_t* out, RadixShared& sh)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nth = blockDim.x;
     uint32_t prefix = 0, mask = 0;
     unsigned need = (unsigned)K;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < RADIX; i += nth) sh.hist[i] = 0;
-        __syncthreads();
-        for (int64_t j = tid; j < n; j += nth) {
-            const uint32_t u = key_at(j);
-            if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & (RADIX - 1)], 1u);
+        if (!HIST0 || shift != 24) {
+            for (int i = tid; i < RADIX; i += nth) sh.hist[i] = 0;
+            __syncthreads();
+            for (int64_t j = tid; j < n; j += nth) {
+                const uint32_t u = key_at(j);
+                if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & (RADIX - 1)], 1u);
+            }
+            __syncthreads();
         }
-        __syncthreads();
         if (warp == 0) radix_find_digit(sh, need);
         __syncthreads();
         prefix |= (uint32_t)sh.digit << shift;
