@@ -617,18 +617,30 @@ def run_ours(args):
                 "traffic": traffic,
                 "step_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
-    # end to end through host buffers: per step copy q, q_idx, w, gate in from
-    # pinned memory, run the step, copy the output back, wait for it
-    host = {k: inp[k].cpu().pin_memory() for k in ("q", "q_idx", "w", "gate")}
+    # end to end through host buffers: per step copy the step's q, q_idx, w
+    # and gate in from one pinned staging buffer (one copy: they sit packed in
+    # one device buffer, each part at a 16-byte offset), run the step through
+    # the API, copy the output back and wait for it
+    names = ("q", "q_idx", "w", "gate")
+    sizes = [inp[k].numel() * inp[k].element_size() for k in names]
+    offs = [sum(sizes[:i]) for i in range(len(sizes))]
+    assert all(o % 16 == 0 for o in offs)
+    dbuf = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+    staged = {}
+    for k_, o, n_ in zip(names, offs, sizes):
+        staged[k_] = dbuf[o:o + n_].view(inp[k_].dtype).view(inp[k_].shape)
+        hbuf[o:o + n_].copy_(inp[k_].cpu().contiguous().view(-1).view(torch.uint8))
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = hbuf.numel()
     d2h = out_h.numel() * out_h.element_size()
     stream = torch.cuda.current_stream()
 
     def e2e_step():
-        for k_, t in host.items():
-            inp[k_].copy_(t, non_blocking=True)
-        step()
+        dbuf.copy_(hbuf, non_blocking=True)
+        sa.sparse_attn_decode(staged["q"], staged["q_idx"], staged["w"], staged["gate"], inp["k_cache"],
+                              inp["v_cache"], inp["k_idx_cache"], inp["seq_start"], inp["ctx_len"],
+                              max_ctx, cfg.K, scale, out=out, idx_out=idx)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
     for _ in range(W):
