@@ -112,6 +112,29 @@ def test_topk_heavy_ties_signed_zeros_and_negatives(sa):
     _topk_case(sa, rows, K)
 
 
+# calls whose rows all fit the shared-memory stage (row stride <= 16384) take
+# the small-CTA kernel; the cases above include a longer row and so do not
+@pytest.mark.parametrize("K", [1, 7, 64, 2048])
+def test_topk_short_rows(sa, K):
+    rng = np.random.default_rng(100 + K)
+    lens = [0, 1, K - 1 if K > 1 else 0, K, K + 1, 2 * K + 3, 5001, 12289, 16384]
+    rows = [rng.standard_normal(n).astype(np.float32) for n in lens]
+    _topk_case(sa, rows, K)
+
+
+def test_topk_short_rows_ties_and_unaligned_stride(sa):
+    rng = np.random.default_rng(6)
+    K = 100
+    rows = [rng.integers(-2, 3, size=5000).astype(np.float32),
+            np.zeros(300, np.float32),
+            np.where(rng.random(700) < 0.5, -0.0, 0.0).astype(np.float32),
+            -np.abs(rng.standard_normal(900)).astype(np.float32),
+            np.repeat(rng.standard_normal(10), 50).astype(np.float32),
+            np.concatenate([np.full(2000, 1.5), np.full(3001, 2.5)]).astype(np.float32)]
+    _topk_case(sa, rows, K, ld=5001)              # odd stride: rows 1.. start off 16-byte boundaries
+    _topk_case(sa, rows, K, ld=16384)
+
+
 def test_topk_long_rows_from_global_memory(sa):
     rng = np.random.default_rng(9)
     rows = [rng.standard_normal(n).astype(np.float32) * 3 for n in (131072, 200001)]
@@ -155,6 +178,10 @@ def _check_prefill_rows(cfg, inp, out, idx, rows):
     ("prefill_8k", dict(L=1500, K=256)),
     ("prefill_128k", dict(L=1300, K=200)),
     ("prefill_8k", dict(L=700, K=1024)),          # K >= n for every row: full causal attention
+    # dense rows below 2K with K not a multiple of the 8-row CTA: CTAs straddle
+    # the start of the masked rows (K) and the end of the dense rows (2K)
+    ("prefill_8k", dict(L=333, K=200)),           # every row on the dense kernel, rows >= 200 masked
+    ("prefill_8k", dict(L=1100, K=257)),          # dense rows 0..513, gathered rows 514..1099
 ])
 def test_prefill_parity(sa, name, over):
     cfg = get_config(name, **over)
