@@ -643,7 +643,7 @@ def run_ours(args):
                               max_ctx, cfg.K, scale, out=out, idx_out=idx)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
-    for _ in range(W):
+    for _ in range(max(W, 20)):              # untimed: the host path settles over the first steps
         e2e_step()
     barrier(dev)
     t0 = time.perf_counter()
