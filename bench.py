@@ -655,7 +655,7 @@ def run_ours(args):
 
     prefill = backward = variants = other_decode = None
     if not args.no_prefill:
-        del host, inp
+        del inp, staged, dbuf, hbuf, out_h
         torch.cuda.empty_cache()
         prefill = [bench_prefill(sa, torch, dev, args.seed + rank, PREFILL_WORKLOAD, 10),
                    bench_prefill(sa, torch, dev, args.seed + rank, "prefill_128k", 2)]
