@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_kept_set, check_outputs, to_host
+from parity import certain_zero_scores, check_kept_set, check_outputs, to_host
 from workloads import get_config, make_prefill
 
 pytestmark = pytest.mark.gpu
@@ -41,6 +41,7 @@ def test_blocks_match_oracle(sa, L, K, B):
     rows = np.arange(L)
     pooled = oracle.pool_keys_bf16(inp["k_idx"], B)
     scores = oracle.indexer(inp["q_idx"], inp["w"], pooled, rows, np.zeros_like(rows), rows // B + 1)
+    cz = certain_zero_scores(inp["q_idx"], inp["w"], pooled, rows, np.zeros_like(rows), rows // B + 1)
     for t in rows:
         valid = idx_h[t][idx_h[t] >= 0]
         n_valid = len(valid)
@@ -51,7 +52,7 @@ def test_blocks_match_oracle(sa, L, K, B):
         assert valid.tolist() == expect, f"row {t}"
         padded = np.full(K // B, -1, dtype=np.int64)
         padded[:len(blocks)] = blocks
-        check_kept_set(padded, scores[t], K // B, f"row {t} blocks")
+        check_kept_set(padded, scores[t], K // B, f"row {t} blocks", cz[t])
     ref = oracle.attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], cfg.dv, inp["gate"], rows,
                         np.zeros_like(rows), idx_h, scale)
     check_outputs(out_h, ref, cfg.attn_dtype, "blocks out")

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_kept_set, check_outputs, to_host
+from parity import certain_zero_scores, check_kept_set, check_outputs, to_host
 from workloads import get_config, make_decode, make_prefill
 
 pytestmark = pytest.mark.gpu
@@ -47,10 +47,12 @@ def test_prefill_full_size(sa, name, n_random):
     rows = _sample_rows(cfg.L, cfg.K, n_random, seed=5)
     idx_h = to_host(idx[torch.as_tensor(rows, device=DEV)]).numpy()
     out_h = to_host(out[torch.as_tensor(rows, device=DEV)]).double().numpy()
-    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows), rows + 1,
-                                inp["q_scale"], inp["k_scale"])
+    args = (inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows), rows + 1, inp["q_scale"],
+            inp["k_scale"])
+    ref_scores = oracle.indexer(*args)
+    cz = certain_zero_scores(*args)
     for i, t in enumerate(rows):
-        check_kept_set(idx_h[i], ref_scores[i], cfg.K, f"{name} row {t}")
+        check_kept_set(idx_h[i], ref_scores[i], cfg.K, f"{name} row {t}", cz[i])
     ref = oracle.attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], cfg.dv, inp["gate"], rows,
                         np.zeros_like(rows), idx_h, scale)
     check_outputs(out_h, ref, cfg.attn_dtype, f"{name} out")
@@ -77,10 +79,12 @@ def test_decode_full_size(sa, name, n_seq):
     idx_h = to_host(idx).numpy()
     out_h = to_host(out).double().numpy()
     starts = inp["seq_start"].numpy()
-    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx_cache"], seqs, starts[seqs], lens[seqs],
-                                inp["q_scale"], inp["k_idx_scale"])
+    args = (inp["q_idx"], inp["w"], inp["k_idx_cache"], seqs, starts[seqs], lens[seqs], inp["q_scale"],
+            inp["k_idx_scale"])
+    ref_scores = oracle.indexer(*args)
+    cz = certain_zero_scores(*args)
     for i, b in enumerate(seqs):
-        check_kept_set(idx_h[b], ref_scores[i], cfg.K, f"{name} seq {b}")
+        check_kept_set(idx_h[b], ref_scores[i], cfg.K, f"{name} seq {b}", cz[i])
     ref = oracle.attend(inp["q"], inp["k_cache"], inp["v_cache"], inp["ld_k"], inp["ld_v"], cfg.dv,
                         inp["gate"], seqs, starts[seqs], idx_h[seqs], scale)
     check_outputs(out_h[seqs], ref, cfg.attn_dtype, f"{name} out")

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_kept_set, check_outputs, to_host
+from parity import certain_zero_scores, check_kept_set, check_outputs, to_host
 from workloads import get_config, make_prefill, quantize_rows_e4m3
 
 pytestmark = pytest.mark.gpu
@@ -55,10 +55,12 @@ def _run(sa, cfg, inp):
 
 def _check_rows(cfg, inp, out, idx, rows):
     rows = np.asarray(sorted(set(int(r) for r in rows)))
-    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows), rows + 1,
-                                inp["q_scale"], inp["k_scale"])
+    args = (inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows), rows + 1, inp["q_scale"],
+            inp["k_scale"])
+    ref_scores = oracle.indexer(*args)
+    cz = certain_zero_scores(*args)
     for i, t in enumerate(rows):
-        check_kept_set(idx[t], ref_scores[i], cfg.K, f"row {t}")
+        check_kept_set(idx[t], ref_scores[i], cfg.K, f"row {t}", cz[i])
     ref = oracle.attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], cfg.dv, inp["gate"],
                         rows, np.zeros_like(rows), idx[rows], 1 / math.sqrt(cfg.dqk))
     check_outputs(out[rows].double().numpy(), ref, cfg.attn_dtype, "prefill out")
@@ -84,6 +86,15 @@ def test_fused_bf16_rows_with_boosted_keys(sa):
     inp = make_prefill(cfg, seed=22)
     out, idx = _run(sa, cfg, inp)
     _check_rows(cfg, inp, out, idx, _rows(49152, cfg.L, 16, 2, extra=(49151, 49152, 51199, 51200, 65535, 30000)))
+
+
+def test_fused_fp8_rows_signed_w(sa):
+    # head weights of either sign through the sampled threshold and the filter pass
+    cfg = get_config("prefill_128k", L=20480)
+    inp = make_prefill(cfg, seed=24)
+    inp["w"] = torch.randn(inp["w"].shape, generator=torch.Generator().manual_seed(6))
+    out, idx = _run(sa, cfg, inp)
+    _check_rows(cfg, inp, out, idx, _rows(16384, cfg.L, 24, 4, extra=(16383, 16384, 18432, 20479, 3000)))
 
 
 def test_fused_rows_whose_sample_misleads_fall_back(sa):

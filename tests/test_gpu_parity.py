@@ -7,8 +7,8 @@ import pytest
 import torch
 
 import oracle
-from parity import (RTOL_SCORE, check_kept_set, check_outputs, check_scores, score_denominators,
-                    to_host)
+from parity import (RTOL_SCORE, certain_zero_scores, check_kept_set, check_outputs, check_scores,
+                    score_denominators, to_host)
 from workloads import get_config, make_decode, make_prefill, quantize_rows_e4m3
 
 pytestmark = pytest.mark.gpu
@@ -29,11 +29,12 @@ def _gen(seed):
     return torch.Generator().manual_seed(seed)
 
 
-def _indexer_inputs(T, N, Hi, di, dtype, seed):
+def _indexer_inputs(T, N, Hi, di, dtype, seed, signed_w=False):
     g = _gen(seed)
     qf = torch.randn((T, Hi, di), generator=g)
     kf = torch.randn((N, di), generator=g)
-    w = torch.softmax(torch.randn((T, Hi), generator=g), -1)
+    w = torch.randn((T, Hi), generator=g)
+    w = w if signed_w else torch.softmax(w, -1)
     if dtype == torch.float8_e4m3fn:
         q, qs = quantize_rows_e4m3(qf)
         k, ks = quantize_rows_e4m3(kf)
@@ -61,6 +62,25 @@ def test_indexer_score(sa, dtype, Hi, di):
         for t in range(T):
             check_scores(got[t, :n[t]], ref[t], den[t], RTOL_SCORE[dtype], f"off={off} t={t}")
             assert np.isnan(got[t, n[t]:]).all(), "positions beyond n_t must stay unwritten"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float8_e4m3fn])
+@pytest.mark.parametrize("Hi,di", [(4, 64), (8, 64), (3, 48)])
+def test_indexer_score_signed_w(sa, dtype, Hi, di):
+    # head weights of either sign (the header allows any real w): scores can be
+    # negative, and a head's ReLU term can cancel another's
+    T, N = 150, 333
+    q, qs, w, k, ks = _indexer_inputs(T, N, Hi, di, dtype, seed=7 + Hi * 100 + di, signed_w=True)
+    assert (w < 0).any() and (w > 0).any()
+    dq = lambda x: None if x is None else x.to(DEV)
+    for off in (0, 120):
+        got = to_host(sa.indexer_score(dq(q), dq(w), dq(k), dq(qs), dq(ks), causal_offset=off)).double().numpy()
+        rows = np.arange(T)
+        n = np.clip(rows + 1 + off, 0, N)
+        ref = oracle.indexer(q, w, k, rows, np.zeros(T), n, qs, ks)
+        den = score_denominators(q, w, k, rows, np.zeros(T), n, qs, ks)
+        for t in range(T):
+            check_scores(got[t, :n[t]], ref[t], den[t], RTOL_SCORE[dtype], f"signed w off={off} t={t}")
 
 
 def test_indexer_all_negative_dots_give_exact_zero(sa):
@@ -164,10 +184,12 @@ def _run_prefill(sa, cfg, inp):
 
 def _check_prefill_rows(cfg, inp, out, idx, rows):
     rows = np.asarray(rows)
-    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows),
-                                rows + 1, inp["q_scale"], inp["k_scale"])
+    args = (inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows), rows + 1, inp["q_scale"],
+            inp["k_scale"])
+    ref_scores = oracle.indexer(*args)
+    cz = certain_zero_scores(*args)
     for i, t in enumerate(rows):
-        check_kept_set(idx[t], ref_scores[i], cfg.K, f"row {t}")
+        check_kept_set(idx[t], ref_scores[i], cfg.K, f"row {t}", cz[i])
     ref = oracle.attend(inp["q"], inp["k"], inp["v"], inp["ld_k"], inp["ld_v"], cfg.dv, inp["gate"],
                         rows, np.zeros_like(rows), idx[rows], 1 / math.sqrt(cfg.dqk))
     check_outputs(out[rows].double().numpy(), ref, cfg.attn_dtype, "prefill out")
@@ -186,6 +208,20 @@ def _check_prefill_rows(cfg, inp, out, idx, rows):
 def test_prefill_parity(sa, name, over):
     cfg = get_config(name, **over)
     inp = make_prefill(cfg, seed=11)
+    out, idx = _run_prefill(sa, cfg, inp)
+    _check_prefill_rows(cfg, inp, out, idx, np.arange(cfg.L))
+
+
+@pytest.mark.parametrize("name,over", [
+    ("prefill_8k", dict(L=1500, K=256)),
+    ("prefill_128k", dict(L=1300, K=200)),
+])
+def test_prefill_parity_signed_w(sa, name, over):
+    # head weights of either sign: many scores are negative, and the K-th best
+    # can be negative or zero
+    cfg = get_config(name, **over)
+    inp = make_prefill(cfg, seed=17)
+    inp["w"] = torch.randn(inp["w"].shape, generator=_gen(18))
     out, idx = _run_prefill(sa, cfg, inp)
     _check_prefill_rows(cfg, inp, out, idx, np.arange(cfg.L))
 
@@ -236,10 +272,12 @@ def _check_decode(cfg, inp, out, idx, seqs=None):
     seqs = np.arange(cfg.B) if seqs is None else np.asarray(seqs)
     lens = np.asarray(inp["lens"])
     starts = inp["seq_start"].numpy()
-    ref_scores = oracle.indexer(inp["q_idx"], inp["w"], inp["k_idx_cache"], seqs, starts[seqs],
-                                lens[seqs], inp["q_scale"], inp["k_idx_scale"])
+    args = (inp["q_idx"], inp["w"], inp["k_idx_cache"], seqs, starts[seqs], lens[seqs], inp["q_scale"],
+            inp["k_idx_scale"])
+    ref_scores = oracle.indexer(*args)
+    cz = certain_zero_scores(*args)
     for i, b in enumerate(seqs):
-        check_kept_set(idx[b], ref_scores[i], cfg.K, f"seq {b}")
+        check_kept_set(idx[b], ref_scores[i], cfg.K, f"seq {b}", cz[i])
     ref = oracle.attend(inp["q"], inp["k_cache"], inp["v_cache"], inp["ld_k"], inp["ld_v"], cfg.dv,
                         inp["gate"], seqs, starts[seqs], idx[seqs], 1 / math.sqrt(cfg.dqk))
     check_outputs(out[seqs].double().numpy(), ref, cfg.attn_dtype, "decode out")
@@ -253,6 +291,14 @@ def _check_decode(cfg, inp, out, idx, seqs=None):
 def test_decode_parity(sa, name, over):
     cfg = get_config(name, **over)
     inp = make_decode(cfg, seed=21)
+    out, idx = _run_decode(sa, cfg, inp)
+    _check_decode(cfg, inp, out, idx)
+
+
+def test_decode_parity_signed_w(sa):
+    cfg = get_config("decode_ragged", B=6, ctx_range=(), ctx_list=(100, 2049, 3000, 4097, 9000, 20000))
+    inp = make_decode(cfg, seed=24)
+    inp["w"] = torch.randn(inp["w"].shape, generator=_gen(25))
     out, idx = _run_decode(sa, cfg, inp)
     _check_decode(cfg, inp, out, idx)
 

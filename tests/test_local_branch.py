@@ -1,7 +1,7 @@
 """Branch fusion with a sliding-window local branch (out = g * sparse +
 (1 - g) * local) on the GPU against the fp64 oracle, through the C ABI. The
-sparse branch's index set is the GPU's own (checked against the oracle's by
-the token-path tests); the fused output is compared over it."""
+sparse branch's index set is checked against the oracle's scores with the
+token path's rule, and the fused output is compared over that set."""
 import math
 
 import numpy as np
@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_outputs, to_host
+from parity import certain_zero_scores, check_kept_set, check_outputs, to_host
 from workloads import get_config, make_prefill
 
 pytestmark = pytest.mark.gpu
@@ -37,6 +37,12 @@ def test_local_fusion_matches_oracle(sa, L, K, W):
     torch.cuda.synchronize()
     rows = np.arange(L)
     idx_h = to_host(idx).numpy()
+    args = (inp["q_idx"], inp["w"], inp["k_idx"], rows, np.zeros_like(rows), rows + 1, inp["q_scale"],
+            inp["k_scale"])
+    ref_scores = oracle.indexer(*args)
+    cz = certain_zero_scores(*args)
+    for t in rows:
+        check_kept_set(idx_h[t], ref_scores[t], K, f"row {t}", cz[t])
     widx = np.full((L, W), -1, dtype=np.int32)
     for t in rows:
         pos = np.arange(max(0, t - W + 1), t + 1)
