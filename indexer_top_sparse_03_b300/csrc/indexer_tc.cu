@@ -50,11 +50,19 @@ namespace {
 
 constexpr int TC_BM = 128;                 // keys per tile (MMA M)
 constexpr int TC_BN = 256;                 // (query, head) pairs per tile (MMA N)
-constexpr int TC_ACC = 512 / TC_BN;        // TMEM accumulator buffers (all 512 columns)
+constexpr int TC_GRP = 2;                  // independent pipelines, one per key-tile parity
 constexpr int TC_GROUP = INDEXER_GROUP;    // key tiles per work item
-constexpr int TC_EPI_WARPS = 16;                          // four per TMEM sub-partition
-constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
-constexpr int TC_EPI_COLS = TC_BN * 4 / TC_EPI_WARPS;     // accumulator columns per epilogue thread
+constexpr int TC_EPI_PER_GRP = 8;          // epilogue warps of a pipeline (two per TMEM sub-partition)
+constexpr int TC_EPI_WARPS = TC_GRP * TC_EPI_PER_GRP;
+// warps 0 / 2: TMA producers of pipelines 0 / 1; warps 1 / 3: their MMA
+// issuers; warp 4: staging; warps 5 ..: epilogue (pipeline 0 first)
+constexpr int TC_STAGE_WARP = 4;
+constexpr int TC_EPI_WARP0 = 5;
+constexpr int TC_THREADS = 32 * (TC_EPI_WARP0 + TC_EPI_WARPS);
+constexpr int TC_EPI_THREADS = 32 * TC_EPI_WARPS;
+constexpr int TC_EPI_COLS = TC_BN * 4 / TC_EPI_PER_GRP;   // accumulator columns per epilogue warp
+static_assert(TC_EPI_PER_GRP % 4 == 0 && TC_EPI_COLS % 32 == 0, "epilogue warps cover TMEM evenly");
+static_assert(TC_GRP * TC_BN <= 512, "one TMEM accumulator per pipeline");
 
 template <int ES, int DI, int HI, bool FILTER = false>
 struct TcCfg {
@@ -65,23 +73,26 @@ struct TcCfg {
     static constexpr int KSTEPS = KB / 32;                 // MMAs per K-block (K = 32 bytes)
     static constexpr int A_BYTES = TC_BM * ROWB;
     static constexpr int B_BYTES = TC_BN * ROWB;
-    static constexpr int STAGES = (A_BYTES <= 16384) ? 4 : 3;
-    static constexpr int B_BUFS = (STAGES * A_BYTES + 2 * B_BYTES <= 160 * 1024) ? 2 : 1;
-    static constexpr int OFF_B = STAGES * A_BYTES;
-    static constexpr int OFF_W = OFF_B + B_BUFS * B_BYTES;
-    static constexpr int OFF_THR = OFF_W + TC_BN * 4;          // filter: TQ thresholds
-    static constexpr int OFF_CNT = OFF_THR + TQ * 4;           // filter: [TQ][4] local counts
+    // key-tile stages per pipeline (filter mode keeps room for its lists)
+    static constexpr int STG = FILTER ? 2 : (A_BYTES <= 8192 ? 4 : (A_BYTES <= 16384 ? 3 : 2));
+    static constexpr int B_BUFS = (TC_GRP * STG * A_BYTES + 2 * B_BYTES <= 176 * 1024) ? 2 : 1;
+    static constexpr int OFF_B = TC_GRP * STG * A_BYTES;
+    static constexpr int OFF_W = OFF_B + B_BUFS * B_BYTES;     // [2][TC_BN] staged head weights
+    static constexpr int OFF_THR = OFF_W + 2 * TC_BN * 4;      // filter: [2][TQ] staged thresholds
+    static constexpr int NSUB = 4 * TC_GRP;                    // sub-lists per query (sub-partition x pipeline)
+    static constexpr int OFF_CNT = OFF_THR + 2 * TQ * 4;       // filter: [TQ][NSUB] sub-list counts
     // filter mode: the local candidate lists
-    static constexpr int OFF_C = (OFF_CNT + TQ * 16 + 1023) / 1024 * 1024;
-    static constexpr int BAR_BYTES = 8 * (2 * STAGES + 4 + 2 * TC_ACC) + 16;
+    static constexpr int OFF_C = (OFF_CNT + TQ * NSUB * 4 + 1023) / 1024 * 1024;
+    static constexpr int BAR_BYTES = 8 * (2 * TC_GRP * STG + 4 + 2 * TC_GRP + 4) + 16;
     static constexpr int SMEM_MAX = 227 * 1024 - 1024;         // opt-in maximum less the alignment slack
     // candidates per query and work item kept in shared memory (filter mode)
     static constexpr int LCAP_FIT = (SMEM_MAX - OFF_C - BAR_BYTES) / (TQ * 8);
-    // a query's list is four sub-lists, one per TMEM sub-partition (each
-    // filled by the one warp that owns those 32 keys of the tile)
-    static constexpr int LCAP = (LCAP_FIT > 1024 ? 1024 : (LCAP_FIT < 4 ? 4 : LCAP_FIT)) / 4 * 4;
-    static constexpr int SUBCAP = LCAP / 4;
-    static constexpr bool FILTER_OK = LCAP_FIT >= 64;          // else filter mode is not offered
+    // a query's list is NSUB sub-lists, each filled by the one warp that owns
+    // those 32 keys of the tiles of one pipeline
+    static constexpr int LCAP = (LCAP_FIT > 1024 ? 1024 : (LCAP_FIT < NSUB ? NSUB : LCAP_FIT)) / NSUB * NSUB;
+    static constexpr int SUBCAP = LCAP / NSUB;
+    // filter mode keeps one count register per query of a warp's slice
+    static constexpr bool FILTER_OK = LCAP_FIT >= 64 && HI >= 4;
     static constexpr int L_BYTES = FILTER && FILTER_OK ? TQ * LCAP * 8 : 0;
     static constexpr int OFF_BAR = OFF_C + L_BYTES;
     // never less than 116 KB, so that two CTAs cannot share an SM (each holds
@@ -89,7 +100,8 @@ struct TcCfg {
     static constexpr int SMEM_NEED = OFF_BAR + BAR_BYTES + 1024;
     static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory");
-    static_assert(SUBCAP * 4 == LCAP, "four whole sub-lists per query");
+    static_assert(SUBCAP * NSUB == LCAP, "whole sub-lists per query");
+    static_assert(HI <= 32 && TC_EPI_COLS % HI == 0, "a warp's columns hold whole queries");
     static constexpr uint32_t IDESC = mma_idesc(ES == 2 ? 1u : 0u, TC_BM, TC_BN);
     static_assert(ROWB % KB == 0 && KB >= 32, "operand rows must be 32, 64 or a multiple of 128 bytes");
 };
@@ -131,6 +143,28 @@ SA_DEVINL void item_next(const IndexerArgs& a, ItemWalk& w)
     w.ng = (item_tiles_total<TQ>(a, w.qi) + TC_GROUP - 1) / TC_GROUP;
 }
 
+// The fp32 value v with score_key(v) == key, as a comparison bound:
+// score_key(s) >= key  <=>  s >= key_threshold(key) for every non-NaN s.
+// Keys at or below the key of -inf admit every score (-inf); keys above the
+// key of +inf admit none (NaN compares false).
+SA_DEVINL float key_threshold(uint32_t key)
+{
+    if (key <= 0x007FFFFFu) return __uint_as_float(0xFF800000u);
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// The registers of a finished TMEM load, passed through an empty asm after
+// the wait, so that no use of them is scheduled before the wait.
+SA_DEVINL void reg_fence32(uint32_t (&r)[32])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
 // Weighted ReLU head sum of one (key, query) score from its HI accumulator
 // columns; w holds the query's HI head weights (16-byte aligned). With four or
 // more heads the sum runs on packed fp32x2 lanes (two heads per instruction).
@@ -138,17 +172,16 @@ template <int HI>
 SA_DEVINL float head_sum(const uint32_t* r, const float* w)
 {
     if constexpr (HI >= 4) {
-        unsigned long long acc2 = 0ull;
+        float2 acc2 = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int h4 = 0; h4 < HI; h4 += 4) {
             const float4 w4 = *reinterpret_cast<const float4*>(w + h4);
-            acc2 = f32x2_fma(f32x2_pack(fmaxf(__uint_as_float(r[h4]), 0.0f), fmaxf(__uint_as_float(r[h4 + 1]), 0.0f)),
-                             f32x2_pack(w4.x, w4.y), acc2);
-            acc2 = f32x2_fma(f32x2_pack(fmaxf(__uint_as_float(r[h4 + 2]), 0.0f), fmaxf(__uint_as_float(r[h4 + 3]), 0.0f)),
-                             f32x2_pack(w4.z, w4.w), acc2);
+            acc2 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(r[h4]), 0.0f), fmaxf(__uint_as_float(r[h4 + 1]), 0.0f)),
+                              make_float2(w4.x, w4.y), acc2);
+            acc2 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(r[h4 + 2]), 0.0f), fmaxf(__uint_as_float(r[h4 + 3]), 0.0f)),
+                              make_float2(w4.z, w4.w), acc2);
         }
-        const float2 s2 = f32x2_unpack(acc2);
-        return s2.x + s2.y;
+        return acc2.x + acc2.y;
     } else {
         float s = 0.0f;
 #pragma unroll
@@ -157,92 +190,76 @@ SA_DEVINL float head_sum(const uint32_t* r, const float* w)
     }
 }
 
-// Epilogue of one accumulator tile for one thread: TC_EPI_COLS columns of its
-// key (TC_EPI_COLS / HI queries). All of them are loaded from TMEM first and
-// the accumulator is released (one arrival per warp) before any arithmetic,
-// so the next MMA into this buffer overlaps the head sums and stores. FULL
-// tiles lie inside every query's causal window; the others test each
-// (query, key) pair: store iff t < T and j < n_t.
-template <int HI, bool FULL, bool FP8>
-SA_DEVINL void epi_tile(uint32_t taddr, const float* w, float ks, float* p, int64_t ld_s, int64_t j,
-                        int t_first, const IndexerArgs& a, uint64_t* empty_bar)
+// Epilogue of one accumulator tile for one warp: its key (TMEM lane) x its
+// TC_EPI_COLS columns (TC_EPI_COLS / HI queries), read in chunks of 32
+// columns. The accumulator is released (one arrival per warp) as soon as the
+// last chunk has arrived in registers, so that the next MMA into this buffer
+// overlaps the last chunk's arithmetic. FULL tiles lie inside every query's
+// causal window; the others test each (query, key) pair: kept iff t < T and
+// j < n_t.
+//
+// Store mode writes the score (a warp writes 32 consecutive keys of one
+// query). Filter mode keeps a pair iff its score reaches the query's
+// threshold: the warp ballots its 32 keys per query and appends the kept ones
+// to its own sub-list of the query (no other warp writes there, so the count
+// is a register of this warp); counts keep growing past subcap (the overflow
+// is detected when the item is written out). Sub-lists of one query lie
+// nsub * subcap entries apart.
+template <int HI, bool FULL, bool FP8, bool FILTER, int NSUB>
+SA_DEVINL void epi_tile(uint32_t taddr, const float* w, const float* thr, float ks, float* p, int64_t ld_s,
+                        int64_t j, int t_first, const IndexerArgs& a, unsigned (&cnt)[TC_EPI_COLS / HI],
+                        unsigned long long* lsub, int subcap, uint64_t* empty_bar)
 {
-    constexpr int QPC = 32 / HI;                       // queries per 32 columns
-    constexpr int CH = TC_EPI_COLS / 32;
-    uint32_t r[CH][32];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) tmem_ld32(taddr + c * 32, r[c]);
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-#pragma unroll
-        for (int qq = 0; qq < QPC; ++qq) {
-            float s = head_sum<HI>(&r[c][qq * HI], w + (c * QPC + qq) * HI);
-            if (FP8) s *= ks;
-            if (FULL) {
-                *p = s;
-            } else {
-                const int t = t_first + c * QPC + qq;
-                if (t < a.T && j < indexer_row_n(a, t)) *p = s;
-            }
-            p += ld_s;
-        }
-    }
-}
-
-// Filter-mode epilogue of one accumulator tile for one thread (one key j,
-// TC_EPI_COLS / HI queries): a pair is kept iff it is inside the query's
-// history and score_key(s) >= thr[q]. The warp ballots its 32 keys per query
-// and appends the kept ones to its own sub-list of the query (no other warp
-// writes there, so the count needs no atomic); counts keep growing past
-// subcap (the overflow is detected when the item is written out).
-template <int HI, bool FULL, bool FP8>
-SA_DEVINL void epi_filter(uint32_t taddr, const float* w, float ks, int64_t j, int t_first,
-                          const IndexerArgs& a, const uint32_t* thr, unsigned* cnt4,
-                          unsigned long long* lsub, int subcap, uint64_t* empty_bar)
-{
-    constexpr int QPC = 32 / HI;
-    constexpr int CH = TC_EPI_COLS / 32;
-    uint32_t r[CH][32];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) tmem_ld32(taddr + c * 32, r[c]);
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
+    constexpr int NCH = TC_EPI_COLS / 32;
+    constexpr int QPC = 32 / HI;                       // queries per 32-column chunk
     const int lane = threadIdx.x & 31;
-    if (lane == 0) mbar_arrive(empty_bar);
     const unsigned below = (1u << lane) - 1u;
+    uint32_t r[32];
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
+    for (int c = 0; c < NCH; ++c) {
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        reg_fence32(r);
+        if (c + 1 == NCH) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar);
+        }
 #pragma unroll
         for (int qq = 0; qq < QPC; ++qq) {
             const int q = c * QPC + qq;
-            float s = head_sum<HI>(&r[c][qq * HI], w + q * HI);
+            float s = head_sum<HI>(r + qq * HI, w + q * HI);
             if (FP8) s *= ks;
-            const uint32_t key = score_key(s);
-            bool pass = key >= thr[q];
+            bool in = true;
             if (!FULL) {
                 const int t = t_first + q;
-                pass = pass && t < a.T && j < indexer_row_n(a, t);
+                in = t < a.T && j < indexer_row_n(a, t);
             }
-            const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-            if (m) {                                   // warp-uniform
-                const unsigned base = cnt4[q * 4];     // this warp's count for query q
-                const unsigned slot = base + (unsigned)__popc(m & below);
-                if (pass && slot < (unsigned)subcap)
-                    lsub[(size_t)q * 4 * subcap + slot] =
-                        ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
-                __syncwarp();
-                if (lane == 0) cnt4[q * 4] = base + (unsigned)__popc(m);
+            if constexpr (!FILTER) {
+                if (in) p[(int64_t)q * ld_s] = s;
+            } else {
+                const bool pass = in && s >= thr[q];
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+                if (m) {                               // warp-uniform
+                    const unsigned slot = cnt[q] + (unsigned)__popc(m & below);
+                    if (pass && slot < (unsigned)subcap)
+                        lsub[(size_t)q * NSUB * subcap + slot] =
+                            ((unsigned long long)score_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+                    cnt[q] += (unsigned)__popc(m);
+                }
             }
         }
     }
 }
 
 
+// Two independent pipelines share the CTA: pipeline g takes the key tiles of
+// parity g (counted over the CTA's whole item range), with its own TMA
+// producer, stage ring, MMA issuer, TMEM accumulator (256 columns each) and
+// eight epilogue warps; the query tile of an item and its staged weights are
+// shared. One pipeline's waits (each mbarrier round trip and each MMA issue
+// costs the single issuing thread hundreds of cycles) then overlap the
+// other's, and its epilogue overlaps the other's MMAs.
 template <int ES, int DI, int HI, bool FILTER>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -250,30 +267,35 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 {
     using C = TcCfg<ES, DI, HI, FILTER>;
     constexpr int TQ = C::TQ;
+    constexpr int STG = C::STG;
+    constexpr int NQ = TC_EPI_COLS / HI;               // queries of one epilogue warp's slice
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
+    uint8_t* sA = smem;                                                 // [TC_GRP][STG] key tiles
     uint8_t* sB = smem + C::OFF_B;
-    float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
-    uint32_t* sThr = reinterpret_cast<uint32_t*>(smem + C::OFF_THR);
-    unsigned* sCnt = reinterpret_cast<unsigned*>(smem + C::OFF_CNT);
+    float* sW = reinterpret_cast<float*>(smem + C::OFF_W);             // [2][TC_BN]
+    float* sThr = reinterpret_cast<float*>(smem + C::OFF_THR);         // [2][TQ]
+    unsigned* sCnt = reinterpret_cast<unsigned*>(smem + C::OFF_CNT);   // [TQ][NSUB]
     unsigned long long* sL = reinterpret_cast<unsigned long long*>(smem + C::OFF_C);   // [TQ][LCAP], filter mode
     constexpr bool filter = FILTER && C::FILTER_OK;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* a_full = bars;                       // [STAGES]
-    uint64_t* a_empty = bars + C::STAGES;          // [STAGES]
-    uint64_t* b_full = bars + 2 * C::STAGES;       // [2]
-    uint64_t* b_empty = b_full + 2;                // [2]
-    uint64_t* acc_full = b_empty + 2;              // [TC_ACC]
-    uint64_t* acc_empty = acc_full + TC_ACC;       // [TC_ACC]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + TC_ACC);
+    uint64_t* a_full = bars;                           // [TC_GRP][STG]
+    uint64_t* a_empty = bars + TC_GRP * STG;           // [TC_GRP][STG]
+    uint64_t* b_full = bars + 2 * TC_GRP * STG;        // [2]
+    uint64_t* b_empty = b_full + 2;                    // [2] (one commit per pipeline)
+    uint64_t* acc_full = b_empty + 2;                  // [TC_GRP]
+    uint64_t* acc_empty = acc_full + TC_GRP;           // [TC_GRP]
+    uint64_t* st_full = acc_empty + TC_GRP;            // [2] staged weights / thresholds ready
+    uint64_t* st_empty = st_full + 2;                  // [2] staged buffer free again
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(st_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::STAGES; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
-        for (int i = 0; i < TC_ACC; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_WARPS); }
+        for (int i = 0; i < TC_GRP * STG; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], TC_GRP); }
+        for (int i = 0; i < TC_GRP; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], TC_EPI_PER_GRP); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&st_full[i], 32); mbar_init(&st_empty[i], TC_EPI_WARPS); }
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_q);
@@ -291,38 +313,50 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     it.end_qi = sched.qi[blockIdx.x + 1];
     it.end_g = sched.g[blockIdx.x + 1];
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp < 4 && (warp & 1) == 0) {
+        // ------------------------------------------------------------ producer of pipeline g
+        const int g = warp >> 1;
         if (lane == 0) {
-            int s = 0, bb = 0;
+            int s = 0, bb = 0, gt = 0;
             uint32_t aph = 0, bph = 0;
+            uint64_t* af = a_full + g * STG;
+            uint64_t* ae = a_empty + g * STG;
+            uint8_t* sAg = sA + (size_t)g * STG * C::A_BYTES;
             for (; it.valid(); item_next<TQ>(a, it)) {
                 const int t0 = a.t_begin + it.qi * TQ;
                 const int ntiles = item_tiles_total<TQ>(a, it.qi);
                 const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
-                if (!mbar_wait(&b_empty[bb], bph ^ 1, &g_tc_error)) break;
-                mbar_arrive_expect_tx(&b_full[bb], C::B_BYTES);
-                uint8_t* bdst = sB + (C::B_BUFS == 2 ? bb : 0) * C::B_BYTES;
-                for (int kb = 0; kb < C::NKB; ++kb)
-                    tma_load_2d(bdst + kb * TC_BN * C::KB, &tm_q, kb * (C::KB / ES), t0 * HI, &b_full[bb]);
+                if (g == 0) {                            // the query tile, for both pipelines
+                    if (!mbar_wait(&b_empty[bb], bph ^ 1, &g_tc_error)) break;
+                    mbar_arrive_expect_tx(&b_full[bb], C::B_BYTES);
+                    uint8_t* bdst = sB + (C::B_BUFS == 2 ? bb : 0) * C::B_BYTES;
+                    for (int kb = 0; kb < C::NKB; ++kb)
+                        tma_load_2d(bdst + kb * TC_BN * C::KB, &tm_q, kb * (C::KB / ES), t0 * HI, &b_full[bb]);
+                    if (C::B_BUFS == 2) { bb ^= 1; if (bb == 0) bph ^= 1; } else { bph ^= 1; }
+                }
                 bool ok = true;
                 for (int kt = k_begin; kt < k_end; ++kt) {
-                    if (!mbar_wait(&a_empty[s], aph ^ 1, &g_tc_error)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&a_full[s], C::A_BYTES);
-                    uint8_t* adst = sA + s * C::A_BYTES;
+                    if ((gt++ & 1) != g) continue;
+                    if (!mbar_wait(&ae[s], aph ^ 1, &g_tc_error)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&af[s], C::A_BYTES);
+                    uint8_t* adst = sAg + s * C::A_BYTES;
                     for (int kb = 0; kb < C::NKB; ++kb)
-                        tma_load_2d(adst + kb * TC_BM * C::KB, &tm_k, kb * (C::KB / ES), kt * TC_BM, &a_full[s]);
-                    if (++s == C::STAGES) { s = 0; aph ^= 1; }
+                        tma_load_2d(adst + kb * TC_BM * C::KB, &tm_k, kb * (C::KB / ES), kt * TC_BM, &af[s]);
+                    if (++s == STG) { s = 0; aph ^= 1; }
                 }
                 if (!ok) break;
-                if (C::B_BUFS == 2) { bb ^= 1; if (bb == 0) bph ^= 1; } else { bph ^= 1; }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ MMA issuer of pipeline g
+        const int g = warp >> 1;
         if (lane == 0) {
-            int s = 0, bb = 0, ab = 0;
+            int s = 0, bb = 0, gt = 0;
             uint32_t aph = 0, bph = 0, acph = 0;
+            uint64_t* af = a_full + g * STG;
+            uint64_t* ae = a_empty + g * STG;
+            const uint32_t sAg = smem_u32(sA + (size_t)g * STG * C::A_BYTES);
+            const uint32_t d = tmem + (uint32_t)(g * TC_BN);
             for (; it.valid(); item_next<TQ>(a, it)) {
                 const int ntiles = item_tiles_total<TQ>(a, it.qi);
                 const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
@@ -331,10 +365,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const uint32_t b_base = smem_u32(sB + (C::B_BUFS == 2 ? bb : 0) * C::B_BYTES);
                 bool ok = true;
                 for (int kt = k_begin; kt < k_end; ++kt) {
-                    if (!mbar_wait(&a_full[s], aph, &g_tc_error) || !mbar_wait(&acc_empty[ab], acph ^ 1, &g_tc_error)) { ok = false; break; }
+                    if ((gt++ & 1) != g) continue;
+                    if (!mbar_wait(&af[s], aph, &g_tc_error) || !mbar_wait(&acc_empty[g], acph ^ 1, &g_tc_error)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
-                    const uint32_t d = tmem + (uint32_t)(ab * TC_BN);
+                    const uint32_t a_base = sAg + s * C::A_BYTES;
 #pragma unroll
                     for (int kb = 0; kb < C::NKB; ++kb) {
 #pragma unroll
@@ -346,25 +380,57 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             else tc_mma_f8(d, ad, bd, C::IDESC, acc);
                         }
                     }
-                    tc_commit(&a_empty[s]);          // smem stage free once these MMAs finish
-                    tc_commit(&acc_full[ab]);        // accumulator ready for the epilogue
-                    if (++s == C::STAGES) { s = 0; aph ^= 1; }
-                    if (++ab == TC_ACC) { ab = 0; acph ^= 1; }
+                    tc_commit(&ae[s]);               // smem stage free once these MMAs finish
+                    tc_commit(&acc_full[g]);         // accumulator ready for the epilogue
+                    if (++s == STG) { s = 0; aph ^= 1; }
+                    acph ^= 1;
                 }
                 if (!ok) break;
-                tc_commit(&b_empty[bb]);
+                tc_commit(&b_empty[bb]);             // this pipeline is done with the query tile
                 if (C::B_BUFS == 2) { bb ^= 1; if (bb == 0) bph ^= 1; } else { bph ^= 1; }
             }
         }
+    } else if (warp == TC_STAGE_WARP) {
+        // ------------------------------------------------------------ staging
+        // Head weights of the item's query tile (FP8: times the query-row
+        // scale) and, in filter mode, its thresholds as fp32 bounds, staged
+        // one item ahead into a double buffer.
+        int sb = 0;
+        uint32_t sph = 0;
+        for (; it.valid(); item_next<TQ>(a, it)) {
+            if (!mbar_wait(&st_empty[sb], sph ^ 1, &g_tc_error)) break;
+            const int t0 = a.t_begin + it.qi * TQ;
+            float* wd = sW + sb * TC_BN;
+            for (int i = lane; i < TC_BN; i += 32) {
+                const int t = t0 + i / HI;
+                float wv = 0.0f;
+                if (t < a.T) {
+                    wv = a.w[(int64_t)t * HI + (i % HI)];
+                    if (ES == 1) wv *= a.q_scale[(int64_t)t * HI + (i % HI)];
+                }
+                wd[i] = wv;
+            }
+            if (filter) {
+                for (int q = lane; q < TQ; q += 32) {
+                    const int t = t0 + q;
+                    sThr[sb * TQ + q] = t < a.T ? key_threshold(a.thr[t - a.t_begin]) : __uint_as_float(0x7FFFFFFFu);
+                }
+            }
+            mbar_arrive(&st_full[sb]);               // one arrival per lane, after its own writes
+            if (++sb == 2) { sb = 0; sph ^= 1; }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int e = threadIdx.x - 64;                 // 0 .. 32 * TC_EPI_WARPS - 1
+        const int e = threadIdx.x - 32 * TC_EPI_WARP0;  // 0 .. TC_EPI_THREADS - 1
+        const int g = (warp - TC_EPI_WARP0) / TC_EPI_PER_GRP;   // pipeline of this warp
         const int sub = warp & 3;                       // TMEM sub-partition of this warp
-        const int half = (warp - 2) >> 2;               // which TC_EPI_COLS columns
+        const int part = ((warp - TC_EPI_WARP0) % TC_EPI_PER_GRP) >> 2;   // which TC_EPI_COLS columns
         const int row = sub * 32 + lane;                // TMEM lane = key within the tile
+        const int col0 = part * TC_EPI_COLS;
+        const int tq_first = col0 / HI;
         const bool fp8 = (ES == 1);
-        int ab = 0;
-        uint32_t acph = 0;
+        int sb = 0, gt = 0;
+        uint32_t acph = 0, sph = 0;
         bool ok = true;
         // After a timed-out wait the loop keeps its shape (same named-barrier
         // count in every epilogue warp) but touches neither TMEM nor memory.
@@ -372,94 +438,89 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int t0 = a.t_begin + it.qi * TQ;
             const int ntiles = item_tiles_total<TQ>(a, it.qi);
             const int k_begin = it.g * TC_GROUP, k_end = min(ntiles, k_begin + TC_GROUP);
-            // head weights of this query tile (FP8: times the query-row scale)
-            asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
-            for (int i = e; i < TC_BN; i += TC_EPI_WARPS * 32) {
-                const int t = t0 + i / HI;
-                float wv = 0.0f;
-                if (t < a.T) {
-                    wv = a.w[(int64_t)t * HI + (i % HI)];
-                    if (fp8) wv *= a.q_scale[(int64_t)t * HI + (i % HI)];
-                }
-                sW[i] = wv;
-            }
-            if (filter && e < TQ) {
-                const int t = t0 + e;
-                sThr[e] = t < a.T ? a.thr[t - a.t_begin] : 0xFFFFFFFFu;
-                reinterpret_cast<uint4*>(sCnt)[e] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
+            if (ok) ok = mbar_wait(&st_full[sb], sph, &g_tc_error);
+            ok = __all_sync(0xffffffffu, ok);
+            const float* w_s = sW + sb * TC_BN + col0;
+            const float* thr_s = sThr + sb * TQ + tq_first;
+            unsigned cnt[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) cnt[q] = 0u;
+            unsigned long long* lc = sL + ((size_t)tq_first * C::NSUB + g * 4 + sub) * C::SUBCAP;
 
             // tiles whose every key is visible to every query of the tile
             // skip the per-query causal mask
             const int64_t n_first = indexer_row_n(a, t0);
             const bool rows_full = t0 + TQ <= a.T;
-            const int tq_first = half * (TC_EPI_COLS / HI);
-            // FP8 key scales are loaded one tile ahead
+            // FP8 key scales are loaded one tile (of this pipeline) ahead
             auto key_scale = [&](int kt) -> float {
                 const int64_t jj = (int64_t)kt * TC_BM + row;
-                return (fp8 && jj < a.N) ? __ldg(a.k_scale + jj) : 1.0f;
+                return (fp8 && kt < k_end && jj < a.N) ? __ldg(a.k_scale + jj) : 1.0f;
             };
-            float ks_next = key_scale(k_begin);
-            for (int kt = k_begin; kt < k_end; ++kt) {
+            const int k_mine = k_begin + ((gt & 1) != g ? 1 : 0);
+            float ks_next = key_scale(k_mine);
+            for (int kt = k_mine; kt < k_end; kt += 2) {
                 const int64_t j = (int64_t)kt * TC_BM + row;
                 const float ks = ks_next;
-                if (fp8 && kt + 1 < k_end) ks_next = key_scale(kt + 1);
+                if (fp8) ks_next = key_scale(kt + 2);
                 const bool full = rows_full && (int64_t)kt * TC_BM + TC_BM <= n_first;
-                if (ok) ok = mbar_wait(&acc_full[ab], acph, &g_tc_error);
+                if (ok) ok = mbar_wait(&acc_full[g], acph, &g_tc_error);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
                     tc_fence_after();
-                    const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(ab * TC_BN + half * TC_EPI_COLS);
-                    const float* w_half = sW + tq_first * HI;
-                    if constexpr (filter) {
-                        // query q's sub-list `sub` starts at sL + (q * 4 + sub) * SUBCAP
-                        unsigned long long* lc = sL + ((size_t)tq_first * 4 + sub) * C::SUBCAP;
-                        unsigned* c4 = sCnt + tq_first * 4 + sub;
-                        if (full)
-                            epi_filter<HI, true, ES == 1>(taddr, w_half, ks, j, t0 + tq_first, a, sThr + tq_first,
-                                                          c4, lc, C::SUBCAP, &acc_empty[ab]);
-                        else
-                            epi_filter<HI, false, ES == 1>(taddr, w_half, ks, j, t0 + tq_first, a, sThr + tq_first,
-                                                           c4, lc, C::SUBCAP, &acc_empty[ab]);
-                    } else {
-                        float* p = a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
-                        if (full)
-                            epi_tile<HI, true, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, 0, a, &acc_empty[ab]);
-                        else
-                            epi_tile<HI, false, ES == 1>(taddr, w_half, ks, p, a.ld_s, j, t0 + tq_first, a,
-                                                         &acc_empty[ab]);
-                    }
+                    const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(g * TC_BN + col0);
+                    float* p = filter ? nullptr : a.scores + (int64_t)(t0 + tq_first - a.t_begin) * a.ld_s + j;
+                    if (full)
+                        epi_tile<HI, true, ES == 1, filter, C::NSUB>(taddr, w_s, thr_s, ks, p, a.ld_s, j, t0 + tq_first,
+                                                                     a, cnt, lc, C::SUBCAP, &acc_empty[g]);
+                    else
+                        epi_tile<HI, false, ES == 1, filter, C::NSUB>(taddr, w_s, thr_s, ks, p, a.ld_s, j, t0 + tq_first,
+                                                                      a, cnt, lc, C::SUBCAP, &acc_empty[g]);
                 }
-                if (++ab == TC_ACC) { ab = 0; acph ^= 1; }
+                acph ^= 1;
             }
+            gt += k_end - k_begin;
+            // the staged weights and thresholds of this item are no longer read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&st_empty[sb]);
+            if (++sb == 2) { sb = 0; sph ^= 1; }
             if constexpr (filter) {
                 // the item's segment: query t0 + q of this item goes to
                 // segment it.g of its row; the count is the true one
-                asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_WARPS * 32) : "memory");
-                constexpr int TPQ = TC_EPI_WARPS * 32 / TQ;           // threads per query
+                if (lane == 0) {
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) sCnt[(tq_first + q) * C::NSUB + g * 4 + sub] = cnt[q];
+                }
+                asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_THREADS) : "memory");
+                constexpr int TPQ = TC_EPI_THREADS / TQ;              // threads per query
+                static_assert(TPQ >= 1, "one thread per query at least");
                 const int q = e / TPQ, k0 = e % TPQ;
                 const int t = t0 + q;
                 if (ok && t < a.T) {
-                    const uint4 c4 = reinterpret_cast<const uint4*>(sCnt)[q];
-                    const unsigned cs[4] = {c4.x, c4.y, c4.z, c4.w};
-                    const unsigned cnt = c4.x + c4.y + c4.z + c4.w;
-                    const bool lost = c4.x > (unsigned)C::SUBCAP || c4.y > (unsigned)C::SUBCAP ||
-                                      c4.z > (unsigned)C::SUBCAP || c4.w > (unsigned)C::SUBCAP;
+                    unsigned cs[C::NSUB];
+                    unsigned cnt_q = 0;
+                    bool lost = false;
+#pragma unroll
+                    for (int sbk = 0; sbk < C::NSUB; ++sbk) {
+                        cs[sbk] = sCnt[q * C::NSUB + sbk];
+                        cnt_q += cs[sbk];
+                        lost = lost || cs[sbk] > (unsigned)C::SUBCAP;
+                    }
                     const int64_t seg = (int64_t)(t - a.t_begin) * a.nseg + it.g;
                     unsigned long long* dst = a.seg_cand + seg * a.cap_seg;
-                    if (!lost && cnt <= (unsigned)a.cap_seg) {
+                    if (!lost && cnt_q <= (unsigned)a.cap_seg) {
                         unsigned off = 0;
 #pragma unroll
-                        for (int sb = 0; sb < 4; ++sb) {
-                            const unsigned long long* src = sL + ((size_t)q * 4 + sb) * C::SUBCAP;
-                            for (unsigned k = k0; k < cs[sb]; k += TPQ) dst[off + k] = src[k];
-                            off += cs[sb];
+                        for (int sbk = 0; sbk < C::NSUB; ++sbk) {
+                            const unsigned long long* src = sL + ((size_t)q * C::NSUB + sbk) * C::SUBCAP;
+                            for (unsigned k = k0; k < cs[sbk]; k += TPQ) dst[off + k] = src[k];
+                            off += cs[sbk];
                         }
                     }
                     // a sub-list that lost pairs makes the segment count as overflowed
-                    if (k0 == 0) a.seg_cnt[seg] = lost ? (unsigned)a.cap_seg + 1u : cnt;
+                    if (k0 == 0) a.seg_cnt[seg] = lost ? (unsigned)a.cap_seg + 1u : cnt_q;
                 }
+                // the lists and counts are refilled by the next item
+                asm volatile("bar.sync 1, %0;" :: "r"(TC_EPI_THREADS) : "memory");
             }
         }
     }
