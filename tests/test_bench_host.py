@@ -65,7 +65,7 @@ def test_reference_arm_on_a_non_zero_rank_does_no_work():
 
 def test_reference_arm_prints_one_line(monkeypatch, capsys):
     # a tiny stand-in workload keeps this fast; the line format is what is checked
-    monkeypatch.setattr(bench, "oracle_sample_decode", lambda cfg, seed, nseq: (0.5, 4))
+    monkeypatch.setattr(bench, "oracle_sample_decode", lambda cfg, seed, nseq: (0.5, 4, 1))
     rc = bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"])
     line = json.loads(capsys.readouterr().out.strip())
     assert rc == 0 and line["impl"] == "reference" and line["unit"] == "tok/s"
