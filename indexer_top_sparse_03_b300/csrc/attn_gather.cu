@@ -33,6 +33,7 @@ constexpr int GA_W = 4;                        // warps per CTA
 constexpr int GA_THREADS = 32 * GA_W;
 constexpr int GA_ROWS = 16;                    // kept rows per warp step (the MMA key tile)
 constexpr float GA_RESCALE = 8.0f;             // lazy-rescale margin (exp2 domain)
+constexpr int GA_PQ = 4;                       // steps whose positions are in flight ahead of their copies
 
 template <int DQK, int DV, int GA_STAGES>
 struct GaCfg {
@@ -120,12 +121,17 @@ attn_gather_kernel(AttnArgs a)
         cp_async_commit();                   // one group per step, empty past the end
     };
 
-    int pos_next = load_pos(0);
+    // positions are fetched GA_PQ steps before their gathers are issued, so
+    // that an index load from L2 never sits between a step and its copies
+    int pq[GA_PQ];
+#pragma unroll
+    for (int i = 0; i < GA_PQ; ++i) pq[i] = load_pos(i);
 #pragma unroll
     for (int k = 0; k < GA_STAGES - 1; ++k) {
-        const int pos = pos_next;
-        pos_next = load_pos(k + 1);
-        issue(k, pos);
+        issue(k, pq[0]);
+#pragma unroll
+        for (int i = 0; i + 1 < GA_PQ; ++i) pq[i] = pq[i + 1];
+        pq[GA_PQ - 1] = load_pos(k + GA_PQ);
     }
     __syncthreads();                         // the Q tile
 
@@ -137,11 +143,10 @@ attn_gather_kernel(AttnArgs a)
     const uint32_t qbase = smem_u32(Qs);
 
     for (int k = 0; k < my_steps; ++k) {
-        {
-            const int pos = pos_next;
-            pos_next = load_pos(k + GA_STAGES);
-            issue(k + GA_STAGES - 1, pos);
-        }
+        issue(k + GA_STAGES - 1, pq[0]);
+#pragma unroll
+        for (int i = 0; i + 1 < GA_PQ; ++i) pq[i] = pq[i + 1];
+        pq[GA_PQ - 1] = load_pos(k + GA_STAGES - 1 + GA_PQ);
         cp_async_wait<GA_STAGES - 1>();      // this lane's copies of step k have landed
         __syncwarp();                        // ... and every lane's
         const uint32_t st = smem_u32(ring + (k % GA_STAGES) * C::WSTAGE);
