@@ -218,8 +218,11 @@ def recorded_traffic(kernel: str, src: str):
 
 def decode_bytes(cfg, lens):
     """Algorithmic bytes of one decode step and of its indexer scan."""
+    import torch
     n = sum(lens)
-    scan = n * cfg.di * 2 + cfg.B * cfg.Hi * (cfg.di * 2 + 4)
+    fp8 = cfg.idx_dtype == torch.float8_e4m3fn
+    es = 1 if fp8 else 2                     # FP8 keys: one code byte per element + a 4-byte row scale
+    scan = n * (cfg.di * es + (4 if fp8 else 0)) + cfg.B * cfg.Hi * (cfg.di * es + 4 + (4 if fp8 else 0))
     kept = sum(min(cfg.K, x) for x in lens)
     row = (cfg.dqk * 2 + cfg.dv * 2) if not cfg.latent else cfg.dqk * 2
     gather = kept * row
@@ -367,12 +370,12 @@ def bench_backward(sa, torch, dev, seed, iters=3):
                          "fp32_alu_frac": tf / FP32_ALU_PEAK_TFLOPS}}
 
 
-def bench_decode_config(sa, torch, dev, seed, name, iters=200):
+def bench_decode_config(sa, torch, dev, seed, name, iters=200, **over):
     """Decode throughput of another decode workload (graph replay of one step)
     and its whole-step fraction of the HBM roofline (the same byte count as the
     headline workload: indexer keys scanned + kept rows + small tensors)."""
     from workloads import get_config, make_decode
-    cfg = get_config(name)
+    cfg = get_config(name, **over)
     inp = make_decode(cfg, seed=seed, device=dev)
     lens = inp["lens"]
     scale = 1 / math.sqrt(cfg.dqk)
@@ -382,7 +385,8 @@ def bench_decode_config(sa, torch, dev, seed, name, iters=200):
     def step():
         sa.sparse_attn_decode(inp["q"], inp["q_idx"], inp["w"], inp["gate"], inp["k_cache"], inp["v_cache"],
                               inp["k_idx_cache"], inp["seq_start"], inp["ctx_len"], max(lens), cfg.K, scale,
-                              dv=cfg.dv, ld_k=inp["ld_k"], ld_v=inp["ld_v"], out=out, idx_out=idx)
+                              dv=cfg.dv, q_scale=inp["q_scale"], k_idx_scale=inp["k_idx_scale"],
+                              ld_k=inp["ld_k"], ld_v=inp["ld_v"], out=out, idx_out=idx)
     for _ in range(3):
         step()
     torch.cuda.synchronize()
@@ -406,7 +410,8 @@ def bench_decode_config(sa, torch, dev, seed, name, iters=200):
     ms = e0.elapsed_time(e1) / iters
     step_bytes, _ = decode_bytes(cfg, lens)
     peak = measured_peaks()["hbm_gbs"]
-    res = {"workload": cfg.name, "B": cfg.B, "ctx_sum": int(sum(lens)), "ms": ms, "tok_s": cfg.B / (ms * 1e-3),
+    res = {"workload": cfg.name, "indexer_dtype": str(cfg.idx_dtype).replace("torch.", ""), "B": cfg.B,
+           "ctx_sum": int(sum(lens)), "ms": ms, "tok_s": cfg.B / (ms * 1e-3),
            "step_bytes": step_bytes, "hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / peak}
     del graph, inp
     torch.cuda.empty_cache()
@@ -669,6 +674,9 @@ def run_ours(args):
         backward = bench_backward(sa, torch, dev, args.seed + rank)
         other_decode = [bench_decode_config(sa, torch, dev, args.seed + rank, n)
                         for n in ("decode_mla", "decode_ragged")]
+        # the 128K point with FP8-e4m3 indexer keys (one fp32 scale per cached row)
+        other_decode.append(bench_decode_config(sa, torch, dev, args.seed + rank, WORKLOAD,
+                                                idx_dtype=torch.float8_e4m3fn))
         variants = bench_variants(sa, torch, dev, args.seed + rank)
         variants["break_even"] = bench_break_even(sa, torch, dev, args.seed + rank)
 

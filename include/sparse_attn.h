@@ -224,10 +224,10 @@ typedef struct {
     int K;
     float softmax_scale;
     int attn_dtype;        /* SA_BF16                                        */
-    int idx_dtype;         /* SA_BF16                                        */
+    int idx_dtype;         /* SA_BF16 or SA_FP8_E4M3                         */
     const void* q;         /* [B, Hq, dqk]                                   */
     const void* q_idx;     /* [B, Hi, di]                                    */
-    const float* q_scale;  /* [B, Hi] (FP8 only)                             */
+    const float* q_scale;  /* [B, Hi] positive row scales (FP8 only)         */
     const float* w;        /* [B, Hi]                                        */
     const float* gate;     /* [B, Hq] gate logits                            */
     const void* k_cache;   /* [rows, ld_k]: keys are the first dqk columns   */
@@ -236,7 +236,7 @@ typedef struct {
                               may alias k_cache (latent row)                 */
     int64_t ld_v;
     const void* k_idx_cache;  /* [rows, di] indexer keys                     */
-    const float* k_idx_scale; /* [rows] (FP8 only)                           */
+    const float* k_idx_scale; /* [rows] positive row scales (FP8 only)       */
     const int64_t* seq_start; /* [B] device: first packed row of sequence b  */
     const int32_t* ctx_len;   /* [B] device: cached rows of sequence b,
                                  clamped to [0, max_ctx] on the device       */
@@ -261,7 +261,11 @@ SA_API size_t sa_decode_workspace_size(const sa_decode_args* args);
  * 256-byte aligned; its contents on entry do not matter.
  * Supported: attn_dtype BF16 with dqk, dv multiples of 16, dqk <= 576,
  * dv <= 512; 1 <= Hq <= 64; idx_dtype BF16 with 1 <= Hi <= 32 and di a
- * multiple of 32 in [32, 256]; ld_k, ld_v multiples of 8; 1 <= K <= 65536;
+ * multiple of 32 in [32, 256], or idx_dtype FP8_E4M3 (e4m3 codes, value =
+ * code * row scale; q_scale and k_idx_scale required, 4-byte aligned) with di
+ * a multiple of 64 in [64, 256]: the FP8 score is
+ * k_idx_scale[j] * sum_h w[b,h] q_scale[b,h] max(0, q8 . k8), as in
+ * indexer_score; ld_k, ld_v multiples of 8; 1 <= K <= 65536;
  * 0 <= max_ctx < 2^31.
  */
 SA_API int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes,

@@ -265,8 +265,10 @@ int check_decode_scalars(const sa_decode_args* a)
     if (!valid_dtype(a->idx_dtype) || !valid_dtype(a->attn_dtype)) return SA_ERR_INVALID_ARG;
     if (a->Hi < 1 || a->di < 1) return SA_ERR_INVALID_ARG;
     if (a->ld_k < a->dqk || a->ld_v < a->dv) return SA_ERR_INVALID_ARG;
-    if (a->attn_dtype != SA_BF16 || a->idx_dtype != SA_BF16) return SA_ERR_UNSUPPORTED;
+    if (a->attn_dtype != SA_BF16) return SA_ERR_UNSUPPORTED;
+    if (a->idx_dtype != SA_BF16 && a->idx_dtype != SA_FP8_E4M3) return SA_ERR_UNSUPPORTED;
     if (a->Hi > 32 || a->di % 32 != 0 || a->di > 256) return SA_ERR_UNSUPPORTED;
+    if (a->idx_dtype == SA_FP8_E4M3 && a->di % 64 != 0) return SA_ERR_UNSUPPORTED;
     if (a->dqk % 16 != 0 || a->dv % 16 != 0 || a->dqk > 576 || a->dv > 512) return SA_ERR_UNSUPPORTED;
     if (a->ld_k % 8 != 0 || a->ld_v % 8 != 0 || a->K > MAX_K || a->Hq > 64) return SA_ERR_UNSUPPORTED;
     if (a->max_ctx >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
@@ -284,6 +286,9 @@ int check_decode(const sa_decode_args* a)
     if (!aligned(a->q, 16) || !aligned(a->q_idx, 16) || !aligned(a->k_cache, 16) ||
         !aligned(a->v_cache, 16) || !aligned(a->k_idx_cache, 16) || !aligned(a->out, 16) ||
         !aligned(a->seq_start, 8) || !aligned(a->ctx_len, 4))
+        return SA_ERR_INVALID_ARG;
+    if (a->idx_dtype == SA_FP8_E4M3 &&
+        (!a->q_scale || !a->k_idx_scale || !aligned(a->q_scale, 4) || !aligned(a->k_idx_scale, 4)))
         return SA_ERR_INVALID_ARG;
     return SA_OK;
 }
@@ -688,6 +693,7 @@ int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes, cu
     if (sa::launch_zero(wsb + lay.hist_off, lay.zero_bytes, stream) != cudaSuccess) return SA_ERR_LAUNCH;
     sa::DecodeScanArgs da{};
     da.q_idx = a.q_idx; da.w = a.w; da.k_idx = a.k_idx_cache; da.seq_start = a.seq_start;
+    da.fp8 = a.idx_dtype == SA_FP8_E4M3; da.q_scale = a.q_scale; da.k_scale = a.k_idx_scale;
     da.ctx_len = a.ctx_len; da.max_ctx = a.max_ctx; da.B = a.B; da.Hi = a.Hi; da.di = a.di;
     da.scores = scores; da.ld_s = lay.ld_s; da.hist = hist;
     da.row_tickets = reinterpret_cast<unsigned*>(wsb + lay.row_tickets_off); da.K = a.K;

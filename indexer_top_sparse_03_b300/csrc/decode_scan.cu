@@ -15,6 +15,13 @@
 // no shared-memory staging, and q's B fragments use the same mapping.
 //   k-step kk, fragment column c  ->  dim 32*(kk/2) + 8*((c%8)/2)
 //                                        + 4*(kk%2) + 2*(c/8) + c%2
+// FP8-e4m3 keys (one fp32 scale per cached row) run the m16n8k32 e4m3 shape
+// with the same byte mapping (a lane's 16-byte piece again feeds two
+// k-steps, now of 32 codes each), which halves the bytes the scan streams.
+// As in the prefill indexer, the query-row scale is folded into the head
+// weight and the key scale multiplies the finished head sum (a positive
+// factor commutes with the ReLU):
+//   s[b, j] = sk[j] * sum_h (w[b,h] sq[b,h]) * max(0, q8[b,h,:] . k8[j,:])
 //
 // Work split: every row is cut into chunks of 1024 keys, and the grid (two
 // CTAs per SM) splits the concatenated chunks of all rows into equal
@@ -26,6 +33,8 @@
 // non-zero bins to the sequence's histogram in global memory once per row it
 // touched: the Top-K step reads that histogram to find the bin of the K-th
 // best score without another pass over the scores.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "topk_core.cuh"
@@ -36,15 +45,16 @@ namespace {
 constexpr int SCAN_THREADS = 256;           // 8 warps
 constexpr int SCAN_CHUNK = 1024;            // keys per chunk; a CTA takes a contiguous run of chunks
 constexpr int SCAN_MAX_B = 2048;            // rows per launch (larger batches take several launches)
-__host__ __device__ constexpr int scan_unroll(int di) { return di <= 64 ? 4 : (di == 128 ? 2 : 1); }   // 16-key groups in flight per warp
+// 16-key groups in flight per warp: about 8 KB of key rows per warp
+__host__ __device__ constexpr int scan_unroll(int row_bytes) { return row_bytes <= 128 ? 4 : (row_bytes == 256 ? 2 : 1); }
 
-template <int DI, int NTH>
-__global__ void __launch_bounds__(SCAN_THREADS)
-decode_scan_kernel(DecodeScanArgs a)
+template <int DI, int NTH, bool FP8>
+__device__ __forceinline__ void decode_scan_body(const DecodeScanArgs& a)
 {
-    constexpr int KS = DI / 16;              // k-steps
-    constexpr int VM = DI / 32;              // 16-byte pieces per key row per lane
-    constexpr int SCAN_UNROLL_DI = scan_unroll(DI);
+    constexpr int RB = FP8 ? DI : 2 * DI;    // bytes per key row
+    constexpr int KS = FP8 ? DI / 32 : DI / 16;   // k-steps
+    constexpr int VM = RB / 64;              // 16-byte pieces per key row per lane
+    constexpr int SCAN_UNROLL_DI = FP8 ? 2 * scan_unroll(2 * DI) : scan_unroll(RB);
     griddep_wait();                          // the zeroed histogram and tickets
     griddep_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -87,15 +97,17 @@ decode_scan_kernel(DecodeScanArgs a)
 
     uint32_t bq[KS][NTH][2];
     float wl[NTH][2];
+    using QT = typename std::conditional<FP8, uint8_t, bf16>::type;
+    constexpr int QPE = 16 / (int)sizeof(QT);  // elements per 16-byte piece
     auto load_query = [&](int bl) {
         const int bg = a.b_begin + bl;
-        const bf16* q = static_cast<const bf16*>(a.q_idx) + (int64_t)bg * a.Hi * DI;
+        const QT* q = static_cast<const QT*>(a.q_idx) + (int64_t)bg * a.Hi * DI;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
 #pragma unroll
             for (int nt = 0; nt < NTH; ++nt) {
                 const int h = nt * 8 + g;
-                const int d = 32 * (kk >> 1) + 8 * t4 + 4 * (kk & 1);
+                const int d = 4 * QPE * (kk >> 1) + QPE * t4 + (QPE / 2) * (kk & 1);
                 uint2 v = make_uint2(0, 0);
                 if (h < a.Hi) v = *reinterpret_cast<const uint2*>(q + h * DI + d);
                 bq[kk][nt][0] = v.x;
@@ -107,7 +119,12 @@ decode_scan_kernel(DecodeScanArgs a)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = nt * 8 + 2 * t4 + e;
-                wl[nt][e] = h < a.Hi ? a.w[(int64_t)bg * a.Hi + h] : 0.0f;
+                float wv = 0.0f;
+                if (h < a.Hi) {
+                    wv = a.w[(int64_t)bg * a.Hi + h];
+                    if constexpr (FP8) wv *= a.q_scale[(int64_t)bg * a.Hi + h];
+                }
+                wl[nt][e] = wv;
             }
         }
     };
@@ -153,18 +170,28 @@ decode_scan_kernel(DecodeScanArgs a)
         const int bg = a.b_begin + b;
         const int64_t j0 = (int64_t)(c - sh_prefix[b]) * a.chunk;
         const int cnt = (int)min64(a.chunk, row_len(b) - j0);
-        const bf16* kb = static_cast<const bf16*>(a.k_idx) + (a.seq_start[bg] + j0) * DI;
+        // key rows in elements of their storage type (bf16, or one e4m3 byte)
+        using KT = typename std::conditional<FP8, uint8_t, bf16>::type;
+        const KT* kb = static_cast<const KT*>(a.k_idx) + (a.seq_start[bg] + j0) * DI;
+        constexpr int PE = 16 / (int)sizeof(KT);     // elements per 16-byte piece
+        const float* ksc = nullptr;
+        if constexpr (FP8) ksc = a.k_scale + a.seq_start[bg] + j0;
         float* sc = a.scores + (int64_t)bg * a.ld_s + j0;
         constexpr int STEP = 8 * 16 * SCAN_UNROLL_DI;   // keys per CTA iteration
         for (int base = warp * 16; base < cnt; base += STEP) {
             uint4 va[SCAN_UNROLL_DI][VM], vb[SCAN_UNROLL_DI][VM];
+            float sa0[FP8 ? SCAN_UNROLL_DI : 1], sa1[FP8 ? SCAN_UNROLL_DI : 1];   // FP8 key scales (lanes with t4 == 0)
 #pragma unroll
             for (int u = 0; u < SCAN_UNROLL_DI; ++u) {
                 const int k0 = base + u * 8 * 16 + g, k1 = k0 + 8;
 #pragma unroll
                 for (int m = 0; m < VM; ++m) {
-                    va[u][m] = k0 < cnt ? ldg_stream16_hint(kb + (int64_t)k0 * DI + 32 * m + 8 * t4, pol) : make_uint4(0, 0, 0, 0);
-                    vb[u][m] = k1 < cnt ? ldg_stream16_hint(kb + (int64_t)k1 * DI + 32 * m + 8 * t4, pol) : make_uint4(0, 0, 0, 0);
+                    va[u][m] = k0 < cnt ? ldg_stream16_hint(kb + (int64_t)k0 * DI + 4 * PE * m + PE * t4, pol) : make_uint4(0, 0, 0, 0);
+                    vb[u][m] = k1 < cnt ? ldg_stream16_hint(kb + (int64_t)k1 * DI + 4 * PE * m + PE * t4, pol) : make_uint4(0, 0, 0, 0);
+                }
+                if constexpr (FP8) {
+                    sa0[u] = (t4 == 0 && k0 < cnt) ? __ldg(ksc + k0) : 0.0f;
+                    sa1[u] = (t4 == 0 && k1 < cnt) ? __ldg(ksc + k1) : 0.0f;
                 }
             }
 #pragma unroll
@@ -181,7 +208,10 @@ decode_scan_kernel(DecodeScanArgs a)
                     af[1] = (kk & 1) ? vb[u][m].z : vb[u][m].x;
                     af[3] = (kk & 1) ? vb[u][m].w : vb[u][m].y;
 #pragma unroll
-                    for (int nt = 0; nt < NTH; ++nt) mma_16816(acc[nt], af, bq[kk][nt][0], bq[kk][nt][1]);
+                    for (int nt = 0; nt < NTH; ++nt) {
+                        if constexpr (FP8) mma_16832_e4m3(acc[nt], af, bq[kk][nt][0], bq[kk][nt][1]);
+                        else mma_16816(acc[nt], af, bq[kk][nt][0], bq[kk][nt][1]);
+                    }
                 }
                 float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
@@ -196,6 +226,10 @@ decode_scan_kernel(DecodeScanArgs a)
                 s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
                 s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
                 const int k0 = base + u * 8 * 16 + g, k1 = k0 + 8;
+                if constexpr (FP8) {
+                    s0 *= sa0[u];
+                    s1 *= sa1[u];
+                }
                 if (t4 == 0) {
                     if (k0 < cnt) { sc[k0] = s0; atomicAdd(&sh_hist[key_bin(score_key(s0))], 1u); }
                     if (k1 < cnt) { sc[k1] = s1; atomicAdd(&sh_hist[key_bin(score_key(s1))], 1u); }
@@ -205,6 +239,22 @@ decode_scan_kernel(DecodeScanArgs a)
         ++done;
     }
     finish_row(b, done);
+}
+
+template <int DI, int NTH>
+__global__ void __launch_bounds__(SCAN_THREADS)
+decode_scan_kernel(DecodeScanArgs a)
+{
+    decode_scan_body<DI, NTH, false>(a);
+}
+
+// FP8 keys: two CTAs per SM are kept for the single n-tile shape (its twice
+// deeper unroll would otherwise take more than half the register file)
+template <int DI, int NTH>
+__global__ void __launch_bounds__(SCAN_THREADS, NTH == 1 ? 2 : 1)
+decode_scan_fp8_kernel(DecodeScanArgs a)
+{
+    decode_scan_body<DI, NTH, true>(a);
 }
 
 __global__ void __launch_bounds__(256)
@@ -221,6 +271,14 @@ cudaError_t launch_di(const DecodeScanArgs& a, cudaStream_t s)
     // about two CTAs per SM, each with an equal share of the rows' chunks
     const int64_t chunks_max = (int64_t)a.nb * ((a.max_ctx + a.chunk - 1) / a.chunk);
     const dim3 grid((unsigned)min64(chunks_max, 2 * (int64_t)device_sm_count()));
+    if (a.fp8) {
+        if constexpr (DI % 64 == 0) {
+            if (a.Hi <= 8) return launch_kernel(decode_scan_fp8_kernel<DI, 1>, grid, dim3(SCAN_THREADS), 0, s, true, a);
+            if (a.Hi <= 16) return launch_kernel(decode_scan_fp8_kernel<DI, 2>, grid, dim3(SCAN_THREADS), 0, s, true, a);
+            return launch_kernel(decode_scan_fp8_kernel<DI, 4>, grid, dim3(SCAN_THREADS), 0, s, true, a);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (a.Hi <= 8) return launch_kernel(decode_scan_kernel<DI, 1>, grid, dim3(SCAN_THREADS), 0, s, true, a);
     if (a.Hi <= 16) return launch_kernel(decode_scan_kernel<DI, 2>, grid, dim3(SCAN_THREADS), 0, s, true, a);
     return launch_kernel(decode_scan_kernel<DI, 4>, grid, dim3(SCAN_THREADS), 0, s, true, a);

@@ -137,9 +137,12 @@ decode_finish_kernel(DecodeSelectArgs a)
     __syncthreads();
     if (!take_bin) {
         // the (K - above)-th largest composite (all distinct); the top 12 bits
-        // of every candidate's key are the bin itself, so the search starts below
+        // of every candidate's key are the bin itself, so the search starts
+        // at the digit of bits 48..55 (its top half is still the bin, equal
+        // for every candidate) and its 8-bit digits end exactly at bit 0: the
+        // low bits of the position decide ties of equal keys
         unsigned long long prefix, mask;
-        radix_kth<unsigned long long>(cs, cnt, (unsigned)K - bs.above, sh, prefix, mask, 64 - HBITS - 8);
+        radix_kth<unsigned long long>(cs, cnt, (unsigned)K - bs.above, sh, prefix, mask, 48);
         prefix |= (unsigned long long)bs.bin << (64 - HBITS);
         mask |= ~0ull << (64 - HBITS);
         for (unsigned i = tid; i < cnt; i += FIN_THREADS) {

@@ -264,9 +264,12 @@ struct BinSplit {
 
 // ---- decode step 1: indexer scan over each sequence's cache --------------
 struct DecodeScanArgs {
-    const void* q_idx;      // [B, Hi, di] bf16
+    const void* q_idx;      // [B, Hi, di] bf16, or e4m3 codes when fp8
     const float* w;         // [B, Hi]
-    const void* k_idx;      // packed [rows, di] bf16
+    const void* k_idx;      // packed [rows, di] bf16, or e4m3 codes when fp8
+    int fp8;                // e4m3 inputs: q_scale [B, Hi] and k_scale [rows] fp32
+    const float* q_scale;
+    const float* k_scale;
     const int64_t* seq_start;
     const int32_t* ctx_len;
     int64_t max_ctx;

@@ -128,15 +128,17 @@ SA_DEVINL void radix_find_digit(RadixShared& sh, unsigned need)
 // MSB-first radix search over cnt values v[0..cnt) in shared memory (8-bit
 // digits): on return, the values v with (v & mask) >= prefix number at least
 // `need`, and exactly `need` when the values are distinct. Whole block.
-// `start_shift` is the lowest bit of the first digit examined: callers that
-// know the values share their top bits start below them (and must then merge
-// those bits into prefix and mask themselves).
+// `start_shift` is the lowest bit of the first digit examined, a multiple of
+// 8 (the digits then end exactly at bit 0): callers that know the values share
+// their top bits start below them (and must then merge those bits into prefix
+// and mask themselves).
 template <typename T>
 __device__ void radix_kth(const T* v, unsigned cnt, unsigned need, RadixShared& sh, T& prefix_out, T& mask_out,
                           int start_shift = (int)sizeof(T) * 8 - 8)
 {
     const int tid = threadIdx.x, nth = blockDim.x;
     T prefix = 0, mask = 0;
+    start_shift = (start_shift + 7) & ~7;    // whole digits down to bit 0
     for (int shift = start_shift; shift >= 0; shift -= 8) {
         for (int i = tid; i < RADIX; i += nth) sh.hist[i] = 0;
         __syncthreads();

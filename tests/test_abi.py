@@ -148,7 +148,10 @@ def test_empty_inputs_are_no_ops(lib):
     (dict(K=0), binding.SA_ERR_INVALID_ARG),
     (dict(max_ctx=-1), binding.SA_ERR_INVALID_ARG),
     (dict(max_ctx=1 << 31), binding.SA_ERR_UNSUPPORTED),
-    (dict(idx_dtype=binding.SA_FP8_E4M3), binding.SA_ERR_UNSUPPORTED),
+    (dict(idx_dtype=binding.SA_FP8_E4M3), binding.SA_ERR_INVALID_ARG),          # scales missing
+    (dict(idx_dtype=binding.SA_FP8_E4M3, q_scale=1 << 20, k_idx_scale=(1 << 20) + 2),
+     binding.SA_ERR_INVALID_ARG),                                                # misaligned scale
+    (dict(idx_dtype=binding.SA_FP8_E4M3, di=96), binding.SA_ERR_UNSUPPORTED),   # FP8 needs di % 64 == 0
     (dict(attn_dtype=binding.SA_F32), binding.SA_ERR_UNSUPPORTED),
     (dict(di=48), binding.SA_ERR_UNSUPPORTED),
     (dict(ctx_len=None), binding.SA_ERR_INVALID_ARG),

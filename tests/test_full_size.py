@@ -58,9 +58,10 @@ def test_prefill_full_size(sa, name, n_random):
     check_outputs(out_h, ref, cfg.attn_dtype, f"{name} out")
 
 
-@pytest.mark.parametrize("name,n_seq", [("decode_mla", 6), ("decode_ragged", 6), ("decode_128k", 4)])
-def test_decode_full_size(sa, name, n_seq):
-    cfg = get_config(name)
+@pytest.mark.parametrize("name,n_seq,over", [("decode_mla", 6, {}), ("decode_ragged", 6, {}), ("decode_128k", 4, {}),
+                                             ("decode_128k", 4, dict(idx_dtype=torch.float8_e4m3fn))])
+def test_decode_full_size(sa, name, n_seq, over):
+    cfg = get_config(name, **over)
     inp = make_decode(cfg, seed=0)
     d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     if inp["v_cache"] is inp["k_cache"]:
@@ -69,7 +70,8 @@ def test_decode_full_size(sa, name, n_seq):
     scale = 1 / math.sqrt(cfg.dqk)
     out = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"],
                                 d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]), cfg.K,
-                                scale, dv=cfg.dv, ld_k=inp["ld_k"], ld_v=inp["ld_v"], idx_out=idx)
+                                scale, dv=cfg.dv, q_scale=d["q_scale"], k_idx_scale=d["k_idx_scale"],
+                                ld_k=inp["ld_k"], ld_v=inp["ld_v"], idx_out=idx)
     torch.cuda.synchronize()
     del d
     lens = np.asarray(inp["lens"])

@@ -262,8 +262,9 @@ def _run_decode(sa, cfg, inp):
     idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=DEV)
     out = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"],
                                 d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]),
-                                cfg.K, 1 / math.sqrt(cfg.dqk), dv=cfg.dv, ld_k=inp["ld_k"],
-                                ld_v=inp["ld_v"], idx_out=idx)
+                                cfg.K, 1 / math.sqrt(cfg.dqk), dv=cfg.dv, q_scale=d["q_scale"],
+                                k_idx_scale=d["k_idx_scale"], ld_k=inp["ld_k"], ld_v=inp["ld_v"],
+                                idx_out=idx)
     torch.cuda.synchronize()
     return to_host(out), to_host(idx).numpy()
 
@@ -287,6 +288,11 @@ def _check_decode(cfg, inp, out, idx, seqs=None):
     ("decode_ragged", dict(B=8, ctx_range=(), ctx_list=(1, 100, 2047, 2048, 2049, 4097, 9000, 0))),
     ("decode_mla", dict(B=5, ctx=6000)),
     ("decode_128k", dict(B=3, ctx=20000, K=512)),
+    # FP8-e4m3 indexer keys with one fp32 scale per cached row
+    ("decode_ragged", dict(B=8, ctx_range=(), ctx_list=(1, 100, 2047, 2048, 2049, 4097, 9000, 0),
+                           idx_dtype=torch.float8_e4m3fn)),
+    ("decode_128k", dict(B=3, ctx=20000, K=512, idx_dtype=torch.float8_e4m3fn, Hi=8)),
+    ("decode_128k", dict(B=2, ctx=5000, K=300, idx_dtype=torch.float8_e4m3fn, di=128, Hi=16)),
 ])
 def test_decode_parity(sa, name, over):
     cfg = get_config(name, **over)
@@ -383,6 +389,40 @@ def test_decode_topk_exactly_k_in_top_bin(sa):
     _, _, idx = _decode_with_indexer(sa, lens, K, lambda n: sign, seed=41)
     for b in range(len(lens)):
         assert np.array_equal(idx[b], keep[b])
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_topk_boundary_between_adjacent_tied_positions(sa, fp8):
+    # the K-th best score is 0 and the boundary falls between two zero-score
+    # positions that differ only in their lowest bits (999 | 1000, 1969 | 1970):
+    # the lower one must be kept, the higher one dropped
+    lens = [5000, 3000, 2050]
+    K = 2000
+    rng = np.random.default_rng(8)
+    sign = np.full(sum(lens), -1.0)
+    keep, start = [], 0
+    for b, n in enumerate(lens):
+        pos = np.arange(n - 1000, n) if b < 2 else np.sort(rng.choice(n, size=30, replace=False))
+        sign[start + pos] = 1.0
+        zeros = np.setdiff1d(np.arange(n), pos)[:K - len(pos)]
+        keep.append(np.sort(np.concatenate([pos, zeros])))
+        start += n
+    cfg = get_config("decode_ragged", B=len(lens), ctx_range=(), ctx_list=tuple(lens), K=K,
+                     idx_dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16)
+    inp = make_decode(cfg, seed=43)
+    e0 = torch.zeros(cfg.di)
+    e0[0] = 1.0
+    kf = torch.as_tensor(sign, dtype=torch.float32)[:, None] * e0[None, :]
+    qf = e0.expand(cfg.B, cfg.Hi, cfg.di).contiguous()
+    if fp8:
+        inp["k_idx_cache"], inp["k_idx_scale"] = quantize_rows_e4m3(kf)
+        inp["q_idx"], inp["q_scale"] = quantize_rows_e4m3(qf)
+    else:
+        inp["k_idx_cache"], inp["q_idx"] = kf.to(torch.bfloat16), qf.to(torch.bfloat16)
+    out, idx = _run_decode(sa, cfg, inp)
+    for b in range(len(lens)):
+        assert np.array_equal(idx[b], keep[b]), f"seq {b}"
+    _check_decode(cfg, inp, out, idx)
 
 
 def test_decode_topk_all_scores_tied(sa):
