@@ -91,6 +91,39 @@ __device__ void combine_splits(const AttnArgs& a, int r, int h0, int h1)
 }
 
 // Ticket: returns true in every thread of the CTA that finished row r's group last.
+// Thread-block cluster helpers: rank in the cluster, a full cluster barrier
+// (release / acquire: shared-memory writes before it are visible to every
+// peer after it), and loads of a peer CTA's shared memory at the address the
+// same variable has in this CTA.
+SA_DEVINL unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+SA_DEVINL void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+SA_DEVINL uint32_t cluster_map(const void* p, unsigned rank)
+{
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(p)), "r"(rank));
+    return d;
+}
+SA_DEVINL float ld_cluster_f32(const float* p, unsigned rank)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_map(p, rank)) : "memory");
+    return v;
+}
+SA_DEVINL float2 ld_cluster_f32x2(const float* p, unsigned rank)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(cluster_map(p, rank)) : "memory");
+    return v;
+}
+
 SA_DEVINL bool take_ticket(unsigned* ticket, int splits, int* sh_flag)
 {
     __threadfence();
