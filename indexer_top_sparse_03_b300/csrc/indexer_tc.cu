@@ -52,6 +52,10 @@ constexpr int TC_BM = 128;                 // keys per tile (MMA M)
 constexpr int TC_BN = 256;                 // (query, head) pairs per tile (MMA N)
 constexpr int TC_GRP = 2;                  // independent pipelines, one per key-tile parity
 constexpr int TC_GROUP = INDEXER_GROUP;    // key tiles per work item
+#ifndef SA_TC_ITEM_COST
+#define SA_TC_ITEM_COST 8
+#endif
+constexpr int TC_ITEM_COST = SA_TC_ITEM_COST;   // scheduling cost of an item beyond its tiles (in tiles)
 constexpr int TC_EPI_PER_GRP = 8;          // epilogue warps of a pipeline (two per TMEM sub-partition)
 constexpr int TC_EPI_WARPS = TC_GRP * TC_EPI_PER_GRP;
 // warps 0 / 2: TMA producers of pipelines 0 / 1; warps 1 / 3: their MMA
@@ -544,13 +548,17 @@ cudaError_t launch_tc_mode(const IndexerArgs& a, cudaStream_t s)
     if (!make_tensor_map_2d(&tk, a.k_idx, ES, a.N, DI, DI, C::KB / ES, TC_BM) ||
         !make_tensor_map_2d(&tq, a.q_idx, ES, (int64_t)a.T * HI, DI, DI, C::KB / ES, TC_BN))
         return cudaErrorNotSupported;
-    // items in (qi, g) order, cut into contiguous ranges of about equal tiles
+    // items in (qi, g) order, cut into contiguous ranges of about equal cost:
+    // a key tile costs one unit and an item TC_ITEM_COST more (its query tile
+    // is loaded and its weights staged once per item, which matters in the
+    // short items at the start of the causal triangle)
     const int nq = (a.T - a.t_begin + C::TQ - 1) / C::TQ;
     int64_t tiles = 0, items = 0;
     for (int qi = 0; qi < nq; ++qi) {
         const int nt = item_tiles_total<C::TQ>(a, qi);
-        tiles += nt;
-        items += (nt + TC_GROUP - 1) / TC_GROUP;
+        const int ng = (nt + TC_GROUP - 1) / TC_GROUP;
+        tiles += nt + (int64_t)ng * TC_ITEM_COST;
+        items += ng;
     }
     if (items == 0) return cudaSuccess;
     const int grid = (int)min64(min64(items, device_sm_count()), TC_MAX_CTAS);
@@ -569,7 +577,7 @@ cudaError_t launch_tc_mode(const IndexerArgs& a, cudaStream_t s)
                 sched.qi[c] = qi;
                 sched.g[c] = g;
             }
-            done += min(TC_GROUP, nt - g * TC_GROUP);
+            done += min(TC_GROUP, nt - g * TC_GROUP) + TC_ITEM_COST;
         }
     }
     for (int k = c + 1; k <= grid; ++k) {    // unused CTAs (and the end marker): past the last item
