@@ -24,17 +24,22 @@ namespace {
 constexpr int AT_THREADS = 128;     // 4 warps
 constexpr int CHUNK = 64;           // kept rows per pipeline stage
 constexpr int PAD = 8;              // bf16 elements of row padding (16 B)
+constexpr int MMA_POS_CAP = 2048;   // kept positions a CTA stages in shared memory
 
 // ---------------------------------------------------------------------------
 // bf16 tensor-core path (mma.sync m16n8k16); dv = 32 * NT, NT even
 // ---------------------------------------------------------------------------
-template <int NT>
+template <int NT, int CH>
 __global__ void __launch_bounds__(AT_THREADS)
 attn_mma_kernel(AttnArgs a)
 {
+    constexpr int KPW = CH / 4;            // keys of a chunk per warp (S = Q K^T)
+    constexpr int NTW = KPW / 8;           // their 8-key n-tiles
+    static_assert(NTW == 1 || NTW == 2, "16 or 8 keys per warp");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ float red_max[4][16], red_sum[4][16];
     __shared__ int sh_flag;
+    __shared__ int spos[MMA_POS_CAP];        // the CTA's kept positions (-1: none), when they fit
 
     griddep_wait();                          // the kept positions
     griddep_launch();
@@ -42,13 +47,13 @@ attn_mma_kernel(AttnArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
     const int dqk = a.dqk, dv = a.dv;
-    const int qs_ld = dqk + PAD, ks_ld = dqk + PAD, vs_ld = dv + PAD, ps_ld = CHUNK + PAD;
+    const int qs_ld = dqk + PAD, ks_ld = dqk + PAD, vs_ld = dv + PAD, ps_ld = CH + PAD;
 
     const int stages = a.stages;
     bf16* Qs = reinterpret_cast<bf16*>(smem_raw);
     bf16* Ks = Qs + 16 * qs_ld;
-    bf16* Vs = Ks + stages * CHUNK * ks_ld;
-    bf16* Ps = Vs + (a.v_aliases_k ? 0 : stages * CHUNK * vs_ld);
+    bf16* Vs = Ks + stages * CH * ks_ld;
+    bf16* Ps = Vs + (a.v_aliases_k ? 0 : stages * CH * vs_ld);
     const int vld = a.v_aliases_k ? ks_ld : vs_ld;
 
     const int64_t n = attn_hist_len(a, r);
@@ -73,26 +78,38 @@ attn_mma_kernel(AttnArgs a)
         }
     }
 
+    // the positions of the CTA's kept rows are staged once, so that no copy
+    // below waits on an index load
+    const bool staged = cnt <= MMA_POS_CAP;
+    if (staged) {
+        for (int i = tid; i < cnt; i += AT_THREADS) {
+            const int pos = sel[begin + i];
+            spos[i] = (pos >= 0 && pos < n) ? pos : -1;
+        }
+        __syncthreads();
+    }
+    auto pos_of = [&](int slot) -> int {
+        if (slot >= end) return -1;
+        if (staged) return spos[slot - begin];
+        const int pos = sel[slot];
+        return (pos >= 0 && pos < n) ? pos : -1;
+    };
+    // a warp copies whole rows (its lanes stride over the row's 16-byte
+    // pieces), so that no per-piece index arithmetic is needed
     auto issue = [&](int c, int buf) {
         const int kpieces = dqk / 8, vpieces = dv / 8;
-        bf16* kdst = Ks + buf * CHUNK * ks_ld;
-        for (int i = tid; i < CHUNK * kpieces; i += AT_THREADS) {
-            const int row = i / kpieces, pc = i % kpieces;
-            const int slot = begin + c * CHUNK + row;
-            int pos = slot < end ? sel[slot] : -1;
-            const bool ok = pos >= 0 && pos < n;
-            const bf16* src = kp + (ok ? (base + pos) * a.ld_k + pc * 8 : 0);
-            cp_async16(kdst + row * ks_ld + pc * 8, src, ok);
-        }
-        if (!a.v_aliases_k) {
-            bf16* vdst = Vs + buf * CHUNK * vs_ld;
-            for (int i = tid; i < CHUNK * vpieces; i += AT_THREADS) {
-                const int row = i / vpieces, pc = i % vpieces;
-                const int slot = begin + c * CHUNK + row;
-                int pos = slot < end ? sel[slot] : -1;
-                const bool ok = pos >= 0 && pos < n;
-                const bf16* src = vp + (ok ? (base + pos) * a.ld_v + pc * 8 : 0);
-                cp_async16(vdst + row * vs_ld + pc * 8, src, ok);
+        bf16* kdst = Ks + buf * CH * ks_ld;
+        bf16* vdst = Vs + buf * CH * vs_ld;
+        for (int row = warp; row < CH; row += AT_THREADS / 32) {
+            const int pos = pos_of(begin + c * CH + row);
+            const bool ok = pos >= 0;
+            const bf16* ksrc = kp + (ok ? (base + pos) * a.ld_k : 0);
+            bf16* kd = kdst + row * ks_ld;
+            for (int pc = lane; pc < kpieces; pc += 32) cp_async16(kd + pc * 8, ksrc + pc * 8, ok);
+            if (!a.v_aliases_k) {
+                const bf16* vsrc = vp + (ok ? (base + pos) * a.ld_v : 0);
+                bf16* vd = vdst + row * vs_ld;
+                for (int pc = lane; pc < vpieces; pc += 32) cp_async16(vd + pc * 8, vsrc + pc * 8, ok);
             }
         }
         cp_async_commit();
@@ -103,7 +120,7 @@ attn_mma_kernel(AttnArgs a)
     for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     const float sl2 = a.softmax_scale * LOG2E;
-    const int nchunks = (cnt + CHUNK - 1) / CHUNK;
+    const int nchunks = (cnt + CH - 1) / CH;
     const int mat = lane >> 3, rr = lane & 7;
     const int colbase = warp * (dv / 4);
 
@@ -119,25 +136,39 @@ attn_mma_kernel(AttnArgs a)
         __syncthreads();
         if (stages >= 2 && c + stages - 1 < nchunks) issue(c + stages - 1, (c + stages - 1) % stages);
 
-        const bf16* Kb = Ks + buf * CHUNK * ks_ld;
-        const bf16* Vb = a.v_aliases_k ? Kb : Vs + buf * CHUNK * vs_ld;
+        const bf16* Kb = Ks + buf * CH * ks_ld;
+        const bf16* Vb = a.v_aliases_k ? Kb : Vs + buf * CH * vs_ld;
 
-        // S = Q K^T for this warp's 16 keys
-        float s[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-        for (int ks = 0; ks < dqk / 16; ++ks) {
-            uint32_t af[4], bfm[4];
-            ldsm_x4(af, smem_u32(Qs + ((mat & 1) * 8 + rr) * qs_ld + ks * 16 + (mat >> 1) * 8));
-            ldsm_x4(bfm, smem_u32(Kb + (warp * 16 + (mat >> 1) * 8 + rr) * ks_ld + ks * 16 + (mat & 1) * 8));
-            mma_16816(s[0], af, bfm[0], bfm[1]);
-            mma_16816(s[1], af, bfm[2], bfm[3]);
+        // S = Q K^T for this warp's KPW keys
+        float s[NTW][4];
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+        if constexpr (NTW == 2) {
+            for (int ks = 0; ks < dqk / 16; ++ks) {
+                uint32_t af[4], bfm[4];
+                ldsm_x4(af, smem_u32(Qs + ((mat & 1) * 8 + rr) * qs_ld + ks * 16 + (mat >> 1) * 8));
+                ldsm_x4(bfm, smem_u32(Kb + (warp * 16 + (mat >> 1) * 8 + rr) * ks_ld + ks * 16 + (mat & 1) * 8));
+                mma_16816(s[0], af, bfm[0], bfm[1]);
+                mma_16816(s[NTW - 1], af, bfm[2], bfm[3]);
+            }
+        } else {
+            // 8 keys per warp: one B load covers two k-steps (dqk % 32 == 0)
+            for (int ks = 0; ks < dqk / 16; ks += 2) {
+                uint32_t af0[4], af1[4], bfm[4];
+                ldsm_x4(af0, smem_u32(Qs + ((mat & 1) * 8 + rr) * qs_ld + ks * 16 + (mat >> 1) * 8));
+                ldsm_x4(af1, smem_u32(Qs + ((mat & 1) * 8 + rr) * qs_ld + (ks + 1) * 16 + (mat >> 1) * 8));
+                ldsm_x4(bfm, smem_u32(Kb + (warp * 8 + rr) * ks_ld + ks * 16 + (mat & 1) * 8 + (mat >> 1) * 16));
+                mma_16816(s[0], af0, bfm[0], bfm[1]);
+                mma_16816(s[0], af1, bfm[2], bfm[3]);
+            }
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int kc = warp * 16 + nt * 8 + 2 * t4 + e;
-                const bool ok = begin + c * CHUNK + kc < end;
+                const int kc = warp * KPW + nt * 8 + 2 * t4 + e;
+                const bool ok = begin + c * CH + kc < end;
                 s[nt][e] = ok ? s[nt][e] * sl2 : -INFINITY;
                 s[nt][2 + e] = ok ? s[nt][2 + e] * sl2 : -INFINITY;
                 mx0 = fmaxf(mx0, s[nt][e]);
@@ -160,13 +191,13 @@ attn_mma_kernel(AttnArgs a)
         m0 = mn0; m1 = mn1;
         float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
             const uint32_t p01 = pack_bf16x2(exp2f(s[nt][0] - ref0), exp2f(s[nt][1] - ref0));
             const uint32_t p23 = pack_bf16x2(exp2f(s[nt][2] - ref1), exp2f(s[nt][3] - ref1));
             const float2 f01 = bf16x2_to_f32x2(p01), f23 = bf16x2_to_f32x2(p23);
             ps0 += f01.x + f01.y;
             ps1 += f23.x + f23.y;
-            const int col = warp * 16 + nt * 8 + 2 * t4;
+            const int col = warp * KPW + nt * 8 + 2 * t4;
             *reinterpret_cast<uint32_t*>(Ps + g * ps_ld + col) = p01;
             *reinterpret_cast<uint32_t*>(Ps + (g + 8) * ps_ld + col) = p23;
         }
@@ -184,7 +215,7 @@ attn_mma_kernel(AttnArgs a)
         }
         // O += P V for this warp's value columns
 #pragma unroll
-        for (int ks = 0; ks < CHUNK / 16; ++ks) {
+        for (int ks = 0; ks < CH / 16; ++ks) {
             uint32_t af[4];
             ldsm_x4(af, smem_u32(Ps + ((mat & 1) * 8 + rr) * ps_ld + ks * 16 + (mat >> 1) * 8));
 #pragma unroll
@@ -343,11 +374,19 @@ attn_simt_kernel(AttnArgs a)
     }
 }
 
+// Kept rows per pipeline stage: 32 for wide rows (the 576-wide latent row),
+// so that two stages and two CTAs fit an SM, else 64.
+int mma_chunk(const AttnArgs& a)
+{
+    return (a.dqk >= 256 && a.dqk % 32 == 0) ? 32 : CHUNK;
+}
+
 size_t mma_smem_bytes(const AttnArgs& a, int stages)
 {
-    return sizeof(bf16) * ((size_t)16 * (a.dqk + PAD) + (size_t)stages * CHUNK * (a.dqk + PAD) +
-                           (a.v_aliases_k ? 0 : (size_t)stages * CHUNK * (a.dv + PAD)) +
-                           16 * (CHUNK + PAD));
+    const size_t ch = (size_t)mma_chunk(a);
+    return sizeof(bf16) * ((size_t)16 * (a.dqk + PAD) + (size_t)stages * ch * (a.dqk + PAD) +
+                           (a.v_aliases_k ? 0 : (size_t)stages * ch * (a.dv + PAD)) +
+                           16 * (ch + PAD));
 }
 
 constexpr size_t MMA_SMEM_LIMIT = 200 * 1024;    // leaves room for static shared memory
@@ -356,10 +395,11 @@ constexpr size_t MMA_SMEM_LIMIT = 200 * 1024;    // leaves room for static share
 // unless that leaves room for only one CTA per SM.
 int attention_stages(const AttnArgs& a)
 {
-    // measured: more CTAs per SM beat a deeper pipeline in one CTA
-    // (the 576-wide latent row: 2 stages, one CTA per SM, 241 us per decode
-    // step at 64 x 32K; 1 stage, two CTAs per SM, 203 us)
-    return mma_smem_bytes(a, 2) <= 110 * 1024 ? 2 : 1;
+    // measured: two CTAs per SM beat a deeper pipeline in one CTA (the
+    // 576-wide latent row with 64-row stages: 2 stages, one CTA per SM, 241 us
+    // per decode step at 64 x 32K; 1 stage, two CTAs per SM, 203 us); with
+    // 32-row stages the latent row gets both: two stages, two CTAs per SM
+    return mma_smem_bytes(a, 2) <= 104 * 1024 ? 2 : 1;     // + 9 KB static: two CTAs per SM
 }
 
 template <int NT>
@@ -367,13 +407,14 @@ cudaError_t launch_mma(AttnArgs a, cudaStream_t s)
 {
     a.stages = attention_stages(a);
     const size_t smem = mma_smem_bytes(a, a.stages);
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = mma_chunk(a) == 32 ? attn_mma_kernel<NT, 32> : attn_mma_kernel<NT, CHUNK>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();                  // do not leave the error latched
         return e;
     }
     dim3 grid(a.rows, a.splits, (a.Hq + 15) / 16);
-    return launch_kernel(attn_mma_kernel<NT>, grid, dim3(AT_THREADS), smem, s, a.pdl, a);
+    return launch_kernel(kern, grid, dim3(AT_THREADS), smem, s, a.pdl, a);
 }
 
 }  // namespace
@@ -388,18 +429,18 @@ bool attention_mma_supported(const AttnArgs& a)
     return true;
 }
 
-// Splits of the kept rows per query row for the decode attention. The
-// self-gathering kernel: about two waves of CTAs on 148 SMs, at least 256
-// kept rows per CTA. The shared-tile kernel (wide latent rows, one CTA per SM
-// at most two): about four waves, at least 128 kept rows per CTA. Both
-// measured against more and fewer splits.
+// Splits of the kept rows per query row for the decode attention: at most
+// about two CTAs per SM (148 SMs) in all, and at least 256 (self-gathering
+// kernel) or 128 (shared-tile kernel) kept rows per CTA, so that each CTA's
+// pipeline streams long enough to hide its fill. Both measured against more
+// and fewer splits.
 int attention_splits(int K, int64_t n_cap, int rows, bool gather_kernel)
 {
     const int64_t kept = min64(K, n_cap);
-    const int target = (gather_kernel ? 2 : 4) * 148;
+    const int target = 2 * 148;
     const int64_t min_per = gather_kernel ? 256 : 128;
     if (kept <= min_per || rows <= 0 || rows >= target) return 1;
-    const int want = (target + rows - 1) / rows;
+    const int want = gather_kernel ? (target + rows - 1) / rows : max(1, target / rows);
     int64_t per = (kept + want - 1) / want;
     per = max64(max64(min_per, (K + MAX_SPLITS - 1) / MAX_SPLITS), per);
     per = (per + CHUNK - 1) / CHUNK * CHUNK;
