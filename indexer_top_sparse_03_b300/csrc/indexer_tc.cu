@@ -274,7 +274,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     constexpr int STG = C::STG;
     constexpr int NQ = TC_EPI_COLS / HI;               // queries of one epilogue warp's slice
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte alignment (the swizzled TMA tiles) by pointer arithmetic on
+    // the shared-memory pointer itself, so that the compiler keeps every
+    // access below in the shared address space (32-bit shared loads and
+    // stores rather than generic ones)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sA = smem;                                                 // [TC_GRP][STG] key tiles
     uint8_t* sB = smem + C::OFF_B;
     float* sW = reinterpret_cast<float*>(smem + C::OFF_W);             // [2][TC_BN]
