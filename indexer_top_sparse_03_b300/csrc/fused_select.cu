@@ -128,12 +128,17 @@ fused_select_kernel(FusedSelectArgs a)
         if (tid == 0) a.fail_list[atomicAdd(a.fail_cnt, 1u)] = r;
         return;
     }
-    // gather the pairs (one warp per segment)
+    // gather the pairs (one warp per segment); the filter pass stores the
+    // score's bits, made the order-preserving key here
     const int warp = tid >> 5, lane = tid & 31;
     for (int g = warp; g < nseg; g += FS_THREADS / 32) {
         const unsigned c = __ldcg(cnt + g);
         const unsigned long long* src = a.seg_cand + ((int64_t)r * a.nseg + g) * a.cap_seg;
-        for (unsigned k = lane; k < c; k += 32) cand[offs[g] + k] = __ldcg(src + k);
+        for (unsigned k = lane; k < c; k += 32) {
+            const unsigned long long v = __ldcg(src + k);
+            cand[offs[g] + k] = ((unsigned long long)score_key(__uint_as_float((uint32_t)(v >> 32))) << 32) |
+                                (v & 0xFFFFFFFFull);
+        }
     }
     uint32_t kmax = 0;
     __syncthreads();

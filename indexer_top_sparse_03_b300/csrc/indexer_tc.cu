@@ -207,7 +207,9 @@ SA_DEVINL float head_sum(const uint32_t* r, const float* w)
 // threshold: the warp ballots its 32 keys per query and appends the kept ones
 // to its own sub-list of the query (no other warp writes there, so the count
 // is a register of this warp); counts keep growing past subcap (the overflow
-// is detected when the item is written out). Sub-lists of one query lie
+// is detected when the item is written out). A kept pair is stored as
+// (score bits << 32 | ~j); the selection turns the bits into the
+// order-preserving key when it gathers the pairs. Sub-lists of one query lie
 // nsub * subcap entries apart.
 template <int HI, bool FULL, bool FP8, bool FILTER, int NSUB>
 SA_DEVINL void epi_tile(uint32_t taddr, const float* w, const float* thr, float ks, float* p, int64_t ld_s,
@@ -248,7 +250,7 @@ SA_DEVINL void epi_tile(uint32_t taddr, const float* w, const float* thr, float 
                     const unsigned slot = cnt[q] + (unsigned)__popc(m & below);
                     if (pass && slot < (unsigned)subcap)
                         lsub[(size_t)q * NSUB * subcap + slot] =
-                            ((unsigned long long)score_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+                            ((unsigned long long)__float_as_uint(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
                     cnt[q] += (unsigned)__popc(m);
                 }
             }

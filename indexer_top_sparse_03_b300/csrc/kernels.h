@@ -83,8 +83,8 @@ struct IndexerArgs {
     // then n_t = min(N, (t >> lg) + 1): every block holding a visible position
     int block_log2;         // 0: off
     // filter mode (thr != null): no score is stored; a (query t, key j) pair
-    // with score_key(s) >= thr[t - t_begin] is appended, as the composite
-    // (score_key << 32 | ~j), to the segment of its work item: segment g of
+    // with score_key(s) >= thr[t - t_begin] is appended, as the pair
+    // (float bits of s << 32 | ~j), to the segment of its work item: segment g of
     // row r holds seg_cnt[r * nseg + g] entries (its true count, possibly above
     // cap_seg, in which case only cap_seg were kept) at
     // seg_cand + (r * nseg + g) * cap_seg
