@@ -447,6 +447,24 @@ def bench_variants(sa, torch, dev, seed, iters=5):
         ms = timed(lambda: sa.sparse_attn_prefill_local(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"],
                                                         inp["w"], inp["gate"], cfg.K, scale, win, out=out))
         res[f"local_{win}"] = {"workload": cfg.name, "window": win, "K": cfg.K, "ms": ms, "tok_s": cfg.L / (ms * 1e-3)}
+    # the attention stage (dense rows below 2K + gathered rows) under each
+    # kernel choice for the gathered rows
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    kernels = {}
+    for name, which in (("mma_sync", sa.ATTN_AUTO), ("tcgen05", sa.ATTN_TCGEN05)):
+        prev = sa.set_prefill_attention_kernel(which)
+        try:
+            times = []
+            for _ in range(iters + 1):
+                sa.sparse_attn_prefill(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], inp["w"],
+                                       inp["gate"], cfg.K, scale, q_scale=inp["q_scale"], k_scale=inp["k_scale"],
+                                       out=out, stage_events=ev)
+                torch.cuda.synchronize()
+                times.append(ev[0].elapsed_time(ev[1]))
+        finally:
+            sa.set_prefill_attention_kernel(prev)
+        kernels[name] = statistics.median(times[1:])
+    res["prefill_attention_kernels"] = {"workload": cfg.name, "attention_ms": kernels}
     return res
 
 

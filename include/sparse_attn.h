@@ -76,13 +76,33 @@ SA_API int sa_version(void);
 
 /*
  * Device-side error bits of the current GPU, ORed since the last reset:
- * SA_DEVERR_WAIT_TIMEOUT = a bounded wait of the tensor-core indexer gave up
- * (its outputs are then incomplete; the kernel returned instead of hanging).
+ * SA_DEVERR_WAIT_TIMEOUT = a bounded wait of a tensor-core kernel (the
+ * indexer, or the prefill attention) gave up (its outputs are then
+ * incomplete; the kernel returned instead of hanging).
  * Synchronises the device. *bits receives the word; reset != 0 clears it.
  * Returns SA_OK or SA_ERR_LAUNCH (the copy failed).
  */
 #define SA_DEVERR_WAIT_TIMEOUT 1u
 SA_API int sa_device_errors(unsigned* bits, int reset);
+
+/*
+ * Kernel for the gathered attention of prefill rows (the exact attention
+ * over the kept rows, "Hybrid Attention Architectures...", section 3.1):
+ *   SA_ATTN_AUTO     (default) cp.async gathers into per-warp rings, S = Q K^T
+ *                    and P V on mma.sync; at 16 query heads per key/value
+ *                    head the gather, not the arithmetic, bounds it, and this
+ *                    kernel hides the gather latency best;
+ *   SA_ATTN_TCGEN05  the tensor-core kernel: tiles of 128 kept rows gathered
+ *                    by eight warps into 128-byte-swizzled shared memory,
+ *                    S^T and O^T accumulated in TMEM by tcgen05.mma; used
+ *                    where it applies (bf16, dqk = dv = 128, Hq a multiple
+ *                    of 16), else the default.
+ * Process-wide, takes effect for later calls; returns the previous choice,
+ * or SA_ERR_INVALID_ARG for an unknown value (the choice is unchanged).
+ */
+#define SA_ATTN_AUTO 0
+#define SA_ATTN_TCGEN05 1
+SA_API int sa_set_prefill_attention_kernel(int which);
 
 /*
  * indexer_score -- step 1 alone (exposed for testing).

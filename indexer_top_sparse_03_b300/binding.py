@@ -76,6 +76,8 @@ def load_library(path: str | None = None):
     lib.sa_version.restype = _I
     lib.sa_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), _I]
     lib.sa_device_errors.restype = _I
+    lib.sa_set_prefill_attention_kernel.argtypes = [_I]
+    lib.sa_set_prefill_attention_kernel.restype = _I
     lib.indexer_score.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P, _I64, _P]
     lib.indexer_score.restype = _I
     lib.topk_select.argtypes = [_P, _I64, _P, _I, _I, _P, _P]
@@ -112,6 +114,18 @@ def device_errors(reset: bool = False) -> int:
     bits = ctypes.c_uint(0)
     _check("sa_device_errors", load_library().sa_device_errors(ctypes.byref(bits), 1 if reset else 0))
     return bits.value
+
+
+ATTN_AUTO, ATTN_TCGEN05 = 0, 1
+
+
+def set_prefill_attention_kernel(which: int) -> int:
+    """Kernel for the gathered attention of prefill rows (ATTN_AUTO or
+    ATTN_TCGEN05), process-wide; returns the previous choice."""
+    prev = load_library().sa_set_prefill_attention_kernel(which)
+    if prev < 0:
+        _check("sa_set_prefill_attention_kernel", prev)
+    return prev
 
 
 def status_string(status: int) -> str:

@@ -360,10 +360,21 @@ const char* sa_status_string(int status)
 
 int sa_version(void) { return 100; }
 
+int sa_set_prefill_attention_kernel(int which)
+{
+    if (which != SA_ATTN_AUTO && which != SA_ATTN_TCGEN05) return SA_ERR_INVALID_ARG;
+    return sa::set_prefill_attention_kernel(which);
+}
+
 int sa_device_errors(unsigned* bits, int reset)
 {
     if (!bits) return SA_ERR_INVALID_ARG;
-    return sa::indexer_device_errors(bits, reset != 0) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+    unsigned idx_bits = 0, attn_bits = 0;
+    if (sa::indexer_device_errors(&idx_bits, reset != 0) != cudaSuccess ||
+        sa::attention_tc_device_errors(&attn_bits, reset != 0) != cudaSuccess)
+        return SA_ERR_LAUNCH;
+    *bits = idx_bits | attn_bits;
+    return SA_OK;
 }
 
 int indexer_score(const void* q_idx, int dtype, const float* q_scale, const float* w,

@@ -11,9 +11,8 @@
 namespace sa {
 
 // 2D TMA descriptor of a row-major matrix of 1-, 2- or 4-byte elements
-// (bytes, bf16, fp32); swizzle = the box's row bytes when 32, 64 or 128,
-// else none.
-// swizzle: the box's inner span picks 128/64/32-byte swizzling (else none)
+// (bytes, bf16, fp32); with swizzle, the box's row bytes (32, 64 or 128)
+// pick the swizzle mode (else none).
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, int64_t rows, int64_t cols,
                         int64_t row_stride_elems, int box_cols, int box_rows, bool swizzle = true);
 int device_sm_count();
@@ -272,7 +271,11 @@ struct AttnArgs {
     bool pdl;               // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);          // picks one of:
-bool attention_gather_supported(const AttnArgs& a);                       // TMA gather4, dv <= 128
+int set_prefill_attention_kernel(int which);          // SA_ATTN_*; returns the previous choice
+bool attention_tc_supported(const AttnArgs& a);       // prefill rows on tcgen05, d = 128
+cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t s);
+cudaError_t attention_tc_device_errors(unsigned* bits, bool reset);   // its bounded-wait error word
+bool attention_gather_supported(const AttnArgs& a);   // cp.async gathers + mma.sync, d = 64 or 128
 cudaError_t launch_attention_gather(const AttnArgs& a, cudaStream_t s);
 int attention_splits(int K, int64_t n_cap, int rows, bool gather_kernel);
 

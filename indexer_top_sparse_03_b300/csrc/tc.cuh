@@ -76,6 +76,22 @@ SA_DEVINL void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y, uint64
         :: "r"(smem_u32(dst)), "l"(m), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
 
+// Gather of four rows: the box (one row high) at inner coordinate x of each of
+// rows y0..y3 lands in smem as four consecutive box rows; with a swizzled map
+// the 16-byte chunks are permuted by the destination address, as for a tiled
+// load of the same rows.
+SA_DEVINL void tma_gather4(void* dst, const CUtensorMap* m, int x, int y0, int y1, int y2, int y3, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        :: "r"(smem_u32(dst)), "l"(m), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later reads
+// of the same bytes by the async proxy (a tensor-core operand).
+SA_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // tcgen05
 // ---------------------------------------------------------------------------
@@ -153,6 +169,28 @@ SA_DEVINL unsigned long long f32x2_fma(unsigned long long a, unsigned long long 
     return d;
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane (32x32b shape), and
+// the matching store.
+SA_DEVINL void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+SA_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+SA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 SA_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored in the
@@ -167,12 +205,25 @@ SA_DEVINL uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t swizzle_bytes)
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (sbo << 32) | (1ull << 46) | (layout << 61);
 }
 
-// Instruction descriptor: fp32 accumulator, A/B K-major, shape M x N.
-// ab_format: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
-__host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, int M, int N)
+// Descriptor of an MN-major operand in the 128-byte-swizzled layout: each
+// 128-byte row holds 64 consecutive M (or N) elements of one K index, 8 such
+// rows (consecutive K) form a 1024-byte atom; `mn_stride` bytes separate the
+// atoms of consecutive 64-element M blocks and `k_stride` bytes the atoms of
+// consecutive 8-row K groups.
+SA_DEVINL uint64_t smem_desc_mnmajor128(uint32_t saddr, uint32_t mn_stride, uint32_t k_stride)
 {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((k_stride >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor: fp32 accumulator, shape M x N, A and B K-major
+// unless a_mn / b_mn (MN-major, 16-bit types only).
+// ab_format: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
+__host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, int M, int N, bool a_mn = false,
+                                                 bool b_mn = false)
+{
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 }  // namespace sa

@@ -250,3 +250,13 @@ def test_dense_argument_errors(lib):
     assert call(args(q=None)) == binding.SA_ERR_INVALID_ARG
     assert call(args(out=f + 8)) == binding.SA_ERR_INVALID_ARG
     assert call(args(L=0)) == binding.SA_OK
+
+
+def test_prefill_attention_kernel_selector(lib):
+    # host-side only: the choice is a process-wide setting, unknown values are
+    # refused and leave it unchanged
+    assert lib.sa_set_prefill_attention_kernel(7) == -1
+    prev = lib.sa_set_prefill_attention_kernel(1)
+    assert prev == 0
+    assert lib.sa_set_prefill_attention_kernel(-1) == -1
+    assert lib.sa_set_prefill_attention_kernel(0) == 1
