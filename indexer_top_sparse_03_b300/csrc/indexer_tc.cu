@@ -16,18 +16,26 @@
 // key's TMEM lane, so the epilogue needs no cross-thread reduction, and its
 // stores are coalesced (a warp writes 32 consecutive keys of one query).
 //
-// Persistent CTAs, one per SM, each walking a static stride of work items
+// Persistent CTAs, one per SM, each walking a contiguous range of work items
 // (query tile, group of up to 8 key tiles; key tiles wholly outside the
-// causal window are never visited). Warp roles:
-//   warp 0      TMA producer: query tile once per item, key tiles through a
-//               ring of shared-memory stages (128-byte-swizzled K-major tiles)
-//   warp 1      TMEM owner (512 columns = two 128x256 fp32 accumulators) and
-//               MMA issuer (one thread, kind::f16 or kind::f8f6f4)
-//   warps 2-17  epilogue: TMEM -> registers, ReLU, weighted head sum, causal
-//               mask, fp32 store; four warps per TMEM sub-partition, each
-//               taking a quarter of the 256 columns
-// Accumulators are double-buffered so that the epilogue of one key tile
-// overlaps the MMAs of the next. Every wait is bounded (see tc.cuh).
+// causal window are never visited) that the host cuts so that every CTA gets
+// about the same number of key tiles. The key tiles of an item alternate
+// between two independent pipelines (even / odd tiles), each with its own
+// stage ring, MMA thread, 128x256 fp32 accumulator (2 x 256 = all 512 TMEM
+// columns) and eight epilogue warps, so that one pipeline's epilogue runs
+// while the other's MMAs fill its accumulator. Warp roles:
+//   warps 0, 2  TMA producers of pipelines 0 / 1: the item's query tile
+//               (shared, double-buffered) and their key tiles through a ring
+//               of 128-byte-swizzled K-major stages
+//   warps 1, 3  MMA issuers (one thread each, kind::f16 or kind::f8f6f4);
+//               warp 1 owns the TMEM allocation
+//   warp 4      staging: the item's head weights (FP8: times the query-row
+//               scale) and, in filter mode, its thresholds, one item ahead
+//   warps 5-20  epilogue, eight per pipeline (two per TMEM sub-partition,
+//               each taking half of the 256 columns): TMEM -> registers
+//               (32 columns per load), ReLU, weighted head sum on packed
+//               fp32x2 FMAs, causal mask, fp32 store
+// Every wait is bounded (see tc.cuh).
 //
 // Filter mode (the indexer fused with the first step of Top-K): instead of
 // storing every score, the epilogue keeps the (key, query) pairs whose score
