@@ -292,6 +292,23 @@ SA_API int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_by
                        cudaStream_t stream);
 
 /*
+ * sparse_attn_decode_host -- one decode step whose per-step inputs come from
+ * host memory and whose output goes back to host memory, all on `stream`:
+ * in_bytes bytes are copied from host_in to dev_in (the caller packs the
+ * step's inputs there: args->q, q_idx, w, gate and, for FP8, q_scale point
+ * into dev_in, which must hold in_bytes bytes), then sparse_attn_decode runs,
+ * then args->out (B * Hq * dv elements of attn_dtype) is copied to host_out.
+ * Asynchronous: the caller waits on the stream (or an event recorded after
+ * this call) before reading host_out or rewriting host_in. Page-locked host
+ * buffers make the copies asynchronous; pageable ones work but block.
+ * Errors: SA_ERR_INVALID_ARG for null host_in / dev_in / host_out or
+ * in_bytes == 0, else those of sparse_attn_decode (checked before anything
+ * is enqueued); SA_ERR_LAUNCH if a copy cannot be enqueued.
+ */
+SA_API int sparse_attn_decode_host(const sa_decode_args* args, const void* host_in, void* dev_in, size_t in_bytes,
+                                   void* host_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Gradients of steps 3-4 over a fixed index set (the training path:
  * "Hybrid Attention Architectures...", section 3.1 -- once the indexer has
  * chosen the set, attention over it is ordinary softmax attention -- and

@@ -90,6 +90,8 @@ def load_library(path: str | None = None):
     lib.sa_decode_workspace_size.restype = _SZ
     lib.sparse_attn_decode.argtypes = [ctypes.POINTER(DecodeArgs), _P, _SZ, _P]
     lib.sparse_attn_decode.restype = _I
+    lib.sparse_attn_decode_host.argtypes = [ctypes.POINTER(DecodeArgs), _P, _P, _SZ, _P, _P, _SZ, _P]
+    lib.sparse_attn_decode_host.restype = _I
     lib.sparse_attn_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), _P]
     lib.sparse_attn_decode_noalloc.restype = _I
     lib.sa_prefill_blocks_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs), _I]
@@ -388,6 +390,61 @@ def sparse_attn_decode(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_sta
                                 _stream(q.device, stream))
     _check("sparse_attn_decode", st)
     return out
+
+
+class DecodeStep:
+    """A decode step prepared once and run many times (a serving loop that
+    reuses the same device buffers): the argument structure, the workspace
+    and the stream are fixed here, so each call is a single sparse_attn_decode
+    call through the C ABI. Arguments as for sparse_attn_decode; the tensors
+    must stay allocated, and their contents may change between calls."""
+
+    def __init__(self, q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len,
+                 max_ctx: int, K: int, softmax_scale: float, dv=None, q_scale=None, k_idx_scale=None,
+                 ld_k=None, ld_v=None, out=None, idx_out=None, workspace=None, stream=None):
+        B, Hq, dqk = q.shape
+        dv = (v_cache.shape[-1] if v_cache is not k_cache else dqk) if dv is None else dv
+        if out is None:
+            out = torch.empty((B, Hq, dv), dtype=q.dtype, device=q.device)
+        self.out = out
+        self._a = decode_args(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len, max_ctx,
+                              K, softmax_scale, dv, out, q_scale, k_idx_scale, ld_k, ld_v, idx_out)
+        self._a.stage_events = None
+        self._lib = load_library()
+        nbytes = self._lib.sa_decode_workspace_size(ctypes.byref(self._a))
+        if nbytes == 0:
+            _check("sparse_attn_decode", self._lib.sparse_attn_decode(ctypes.byref(self._a), None, 0, None))
+        self._ws = workspace if workspace is not None else torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                                                                          device=q.device)
+        self._ws_bytes = self._ws.numel() * self._ws.element_size()
+        if self._ws_bytes < nbytes:
+            raise SparseAttnError("workspace", SA_ERR_WORKSPACE)
+        self._ws_ptr = _ptr(self._ws)
+        self._stream = _stream(q.device, stream)
+        # the tensors whose addresses the structure holds
+        self._keep = (q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len, q_scale,
+                      k_idx_scale, idx_out)
+
+    def __call__(self):
+        _check("sparse_attn_decode",
+               self._lib.sparse_attn_decode(ctypes.byref(self._a), self._ws_ptr, self._ws_bytes, self._stream))
+        return self.out
+
+    def run_host(self, host_in, dev_in, host_out):
+        """One step with host buffers (sparse_attn_decode_host): host_in's bytes
+        go to dev_in (the device buffer this step's q, q_idx, w, gate and
+        q_scale live in), the step runs, and the output lands in host_out
+        (page-locked CPU tensors for asynchronous copies). Asynchronous on the
+        step's stream; returns host_out."""
+        if host_in.is_cuda or host_out.is_cuda:
+            raise ValueError("host_in and host_out must be CPU tensors")
+        nbytes = host_in.numel() * host_in.element_size()
+        if host_out.numel() * host_out.element_size() < self.out.numel() * self.out.element_size():
+            raise ValueError("host_out is smaller than the output")
+        _check("sparse_attn_decode_host",
+               self._lib.sparse_attn_decode_host(ctypes.byref(self._a), host_in.data_ptr(), _ptr(dev_in), nbytes,
+                                                 host_out.data_ptr(), self._ws_ptr, self._ws_bytes, self._stream))
+        return host_out
 
 
 def sparse_attn_decode_noalloc(q, q_idx, w, gate, k_cache, v_cache, k_idx_cache, seq_start, ctx_len,

@@ -734,4 +734,27 @@ int sparse_attn_decode(const sa_decode_args* args, void* ws, size_t ws_bytes, cu
     return SA_OK;
 }
 
+int sparse_attn_decode_host(const sa_decode_args* args, const void* host_in, void* dev_in, size_t in_bytes,
+                            void* host_out, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    NvtxRange range("sparse_attn_decode_host");
+    if (!host_in || !dev_in || !host_out || in_bytes == 0) return SA_ERR_INVALID_ARG;
+    int st = check_decode(args);
+    if (st != SA_OK) return st;
+    const sa_decode_args& a = *args;
+    if (a.B > 0) {
+        const DecodeLayout lay = decode_layout(a);
+        if (!ws || ws_bytes < lay.total || !aligned(ws, WS_ALIGN)) return SA_ERR_WORKSPACE;
+    }
+    if (cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SA_ERR_LAUNCH;
+    st = sparse_attn_decode(args, ws, ws_bytes, stream);
+    if (st != SA_OK) return st;
+    const size_t es = a.attn_dtype == SA_BF16 ? 2 : 4;
+    const size_t out_bytes = (size_t)a.B * a.Hq * a.dv * es;
+    if (out_bytes && cudaMemcpyAsync(host_out, a.out, out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return SA_ERR_LAUNCH;
+    return SA_OK;
+}
+
 }  // extern "C"

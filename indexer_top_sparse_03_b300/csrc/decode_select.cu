@@ -40,7 +40,9 @@ SA_DEVINL int64_t row_len(const DecodeSelectArgs& a, int b)
     return n < 0 ? 0 : (n > a.max_ctx ? a.max_ctx : n);
 }
 
-__global__ void __launch_bounds__(BM_THREADS)
+// four CTAs per SM (at most 64 registers): the 512 CTAs of a 32 x 131072
+// batch then run in one wave instead of two
+__global__ void __launch_bounds__(BM_THREADS, 4)
 decode_bitmap_kernel(DecodeSelectArgs a)
 {
     griddep_wait();                          // scores, bins and counters of the scan

@@ -260,3 +260,18 @@ def test_prefill_attention_kernel_selector(lib):
     assert prev == 0
     assert lib.sa_set_prefill_attention_kernel(-1) == -1
     assert lib.sa_set_prefill_attention_kernel(0) == 1
+
+
+def test_decode_host_argument_errors(lib):
+    # null host or device buffers and an empty input copy are refused before
+    # anything is enqueued (no GPU needed)
+    a = binding.DecodeArgs()
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    assert lib.sparse_attn_decode_host(ctypes.byref(a), None, p, 64, p, None, 0, None) == -1
+    assert lib.sparse_attn_decode_host(ctypes.byref(a), p, None, 64, p, None, 0, None) == -1
+    assert lib.sparse_attn_decode_host(ctypes.byref(a), p, p, 64, None, None, 0, None) == -1
+    assert lib.sparse_attn_decode_host(ctypes.byref(a), p, p, 0, p, None, 0, None) == -1
+    # and a bad argument structure fails as sparse_attn_decode would
+    assert lib.sparse_attn_decode_host(ctypes.byref(a), p, p, 64, p, None, 0, None) == \
+        lib.sparse_attn_decode(ctypes.byref(a), None, 0, None)

@@ -301,6 +301,63 @@ def test_decode_parity(sa, name, over):
     _check_decode(cfg, inp, out, idx)
 
 
+def test_decode_prepared_step_matches_the_call(sa):
+    # DecodeStep builds the argument structure once; each call must give what
+    # sparse_attn_decode gives on the buffers' current contents
+    cfg = get_config("decode_ragged", B=6, ctx_range=(), ctx_list=(1, 2047, 2049, 5000, 9000, 0))
+    inp = make_decode(cfg, seed=23)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=DEV)
+    step = sa.DecodeStep(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"], d["k_idx_cache"],
+                         d["seq_start"], d["ctx_len"], max(inp["lens"]), cfg.K, 1 / math.sqrt(cfg.dqk),
+                         q_scale=d["q_scale"], k_idx_scale=d["k_idx_scale"], idx_out=idx)
+    for seed in (0, 1):
+        if seed:                                  # new contents in the same buffers
+            d["q"].copy_(torch.randn(d["q"].shape, generator=_gen(24)).to(d["q"].dtype))
+            d["q_idx"].copy_(torch.randn(d["q_idx"].shape, generator=_gen(25)).to(d["q_idx"].dtype))
+        got = step().clone()
+        got_idx = idx.clone()
+        ref = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"],
+                                    d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]), cfg.K,
+                                    1 / math.sqrt(cfg.dqk), q_scale=d["q_scale"], k_idx_scale=d["k_idx_scale"],
+                                    idx_out=idx)
+        torch.cuda.synchronize()
+        assert torch.equal(got_idx, idx)
+        assert torch.equal(got, ref)
+    inp["q"], inp["q_idx"] = to_host(d["q"]), to_host(d["q_idx"])
+    _check_decode(cfg, inp, to_host(got), to_host(got_idx).numpy())
+
+
+def test_decode_step_with_host_buffers(sa):
+    # sparse_attn_decode_host: the packed per-step inputs come from pinned host
+    # memory and the output goes back there; it must equal the device call
+    cfg = get_config("decode_ragged", B=5, ctx_range=(), ctx_list=(3, 2048, 2049, 7000, 0))
+    inp = make_decode(cfg, seed=26)
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    names = ("q", "q_idx", "w", "gate")
+    sizes = [inp[k].numel() * inp[k].element_size() for k in names]
+    offs = [sum(sizes[:i]) for i in range(len(sizes))]
+    dev_in = torch.empty(sum(sizes), dtype=torch.uint8, device=DEV)
+    host_in = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+    view = {}
+    for k, o, n in zip(names, offs, sizes):
+        view[k] = dev_in[o:o + n].view(inp[k].dtype).view(inp[k].shape)
+        host_in[o:o + n].copy_(inp[k].contiguous().view(-1).view(torch.uint8))
+    idx = torch.empty((cfg.B, cfg.K), dtype=torch.int32, device=DEV)
+    step = sa.DecodeStep(view["q"], view["q_idx"], view["w"], view["gate"], d["k_cache"], d["v_cache"],
+                         d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]), cfg.K,
+                         1 / math.sqrt(cfg.dqk), idx_out=idx)
+    host_out = torch.empty((cfg.B, cfg.Hq, cfg.dv), dtype=torch.bfloat16).pin_memory()
+    step.run_host(host_in, dev_in, host_out)
+    torch.cuda.synchronize()
+    ref = sa.sparse_attn_decode(d["q"], d["q_idx"], d["w"], d["gate"], d["k_cache"], d["v_cache"],
+                                d["k_idx_cache"], d["seq_start"], d["ctx_len"], max(inp["lens"]), cfg.K,
+                                1 / math.sqrt(cfg.dqk))
+    torch.cuda.synchronize()
+    assert torch.equal(host_out, to_host(ref))
+    _check_decode(cfg, inp, host_out, to_host(idx).numpy())
+
+
 def test_decode_parity_signed_w(sa):
     cfg = get_config("decode_ragged", B=6, ctx_range=(), ctx_list=(100, 2049, 3000, 4097, 9000, 20000))
     inp = make_decode(cfg, seed=24)
