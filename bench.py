@@ -742,6 +742,8 @@ def main(argv=None):
     p.add_argument("--profile-prefill", type=int, default=0, metavar="L",
                    help="for profiler captures only: run the FP8 128K-prefill shapes at length L\n"
                         "(--steps calls, no timing, no JSON line) and exit")
+    p.add_argument("--prefill-attention", choices=("auto", "tcgen05"), default="auto",
+                   help="with --profile-prefill: the kernel for the gathered attention of prefill rows")
     args = p.parse_args(argv)
     if args.profile_prefill:
         return profile_prefill(args)
@@ -760,6 +762,7 @@ def profile_prefill(args):
     import indexer_top_sparse_03_b300 as sa
     from workloads import get_config, make_prefill
     sa.load_library()
+    sa.set_prefill_attention_kernel(sa.ATTN_TCGEN05 if args.prefill_attention == "tcgen05" else sa.ATTN_AUTO)
     cfg = get_config("prefill_128k", L=args.profile_prefill)
     inp = make_prefill(cfg, seed=args.seed, device="cuda")
     out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device="cuda")
