@@ -369,11 +369,12 @@ int sa_set_prefill_attention_kernel(int which)
 int sa_device_errors(unsigned* bits, int reset)
 {
     if (!bits) return SA_ERR_INVALID_ARG;
-    unsigned idx_bits = 0, attn_bits = 0;
+    unsigned idx_bits = 0, attn_bits = 0, dense_bits = 0;
     if (sa::indexer_device_errors(&idx_bits, reset != 0) != cudaSuccess ||
-        sa::attention_tc_device_errors(&attn_bits, reset != 0) != cudaSuccess)
+        sa::attention_tc_device_errors(&attn_bits, reset != 0) != cudaSuccess ||
+        sa::attention_dense_tc_device_errors(&dense_bits, reset != 0) != cudaSuccess)
         return SA_ERR_LAUNCH;
-    *bits = idx_bits | attn_bits;
+    *bits = idx_bits | attn_bits | dense_bits;
     return SA_OK;
 }
 

@@ -230,6 +230,10 @@ bool attention_dense_supported(const DenseArgs& a)
 cudaError_t launch_attention_dense(const DenseArgs& a, cudaStream_t s)
 {
     if (a.L <= 0) return cudaSuccess;
+    if (attention_dense_tc_supported(a)) {
+        const cudaError_t e = launch_attention_dense_tc(a, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return a.D == 64 ? launch_dense_d<64>(a, s) : launch_dense_d<128>(a, s);
 }
 

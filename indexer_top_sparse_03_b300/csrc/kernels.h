@@ -197,7 +197,10 @@ struct DenseArgs {
     int64_t mask_from;
 };
 bool attention_dense_supported(const DenseArgs& a);
-cudaError_t launch_attention_dense(const DenseArgs& a, cudaStream_t s);
+cudaError_t launch_attention_dense(const DenseArgs& a, cudaStream_t s);   // tcgen05 where it applies
+bool attention_dense_tc_supported(const DenseArgs& a);                     // d = 128, 16 heads
+cudaError_t launch_attention_dense_tc(const DenseArgs& a, cudaStream_t s);
+cudaError_t attention_dense_tc_device_errors(unsigned* bits, bool reset);
 
 // ---- sliding-window local branch ---------------------------------------------
 // idx[r] = positions max(0, t - W + 1) .. t (t = t0 + r), ascending, W per row
