@@ -19,10 +19,11 @@
 //     computed while the softmax of tile j runs;
 //   - warps 2..5: the softmax, one TMEM lane quarter each: scale to the exp2
 //     domain, causal mask (and, for rows t >= mask_from, the kept-position
-//     bitmap), row maximum, P = exp2(s - m) in bf16 to shared memory as the
-//     K-major A operand of the PV product, row sum of the same rounded
-//     values. A row's maximum is raised only when a score exceeds it by more
-//     than 2^8 (then the thread's O row in TMEM and its sum are rescaled,
+//     bitmap), row maximum, P = exp2(s - m) (the ex2.approx unit) in bf16 to
+//     shared memory as the K-major A operand of the PV product, row sum of
+//     the same rounded values. A row's maximum is raised only when a score
+//     exceeds it by more than 2^8 (then the thread's O row in TMEM and its
+//     sum are rescaled,
 //     which does not change the result); at the end the gate and the bf16
 //     store of the thread's row.
 #include "attn_common.cuh"
@@ -61,6 +62,14 @@ static_assert(DT_OFF_KV % 1024 == 0 && DT_OFF_P % 1024 == 0 && DT_STAGE % 1024 =
 
 constexpr uint32_t DT_IDESC_QK = mma_idesc(1u, DT_M, DT_N);                          // A = Q, B = K (K-major)
 constexpr uint32_t DT_IDESC_PV = mma_idesc(1u, DT_M, DT_D, false, /*b_mn=*/true);    // A = P, B = V (MN-major)
+
+// 2^x by the special-function unit (PTX ex2.approx, flush-to-zero; 2^-inf = 0)
+SA_DEVINL float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 SA_DEVINL void bar_soft() { asm volatile("bar.sync 1, %0;" :: "r"(DT_EPI) : "memory"); }
 
@@ -229,13 +238,21 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const int64_t lim = t - j0;                            // keys c <= lim are visible
             if (lim < 63) keep &= lim < 0 ? 0ull : ((2ull << lim) - 1ull);
             if (t >= a.L) keep = 0ull;
+            // the row maximum on the raw scores (the scale is positive); masked
+            // keys become -inf, which the exponential below maps to 0
             float tmax = -INFINITY;
+            if (__all_sync(0xffffffffu, keep == ~0ull)) {
 #pragma unroll
-            for (int c = 0; c < DT_N; ++c) {
-                const float s = ((keep >> c) & 1ull) ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-                sr[c] = __float_as_uint(s);
-                tmax = fmaxf(tmax, s);
+                for (int c = 0; c < DT_N; ++c) tmax = fmaxf(tmax, __uint_as_float(sr[c]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < DT_N; ++c) {
+                    const float x = ((keep >> c) & 1ull) ? __uint_as_float(sr[c]) : -INFINITY;
+                    sr[c] = __float_as_uint(x);
+                    tmax = fmaxf(tmax, x);
+                }
             }
+            tmax *= sl2;
             const bool need = tmax > m + DT_RESCALE;
             if (__any_sync(0xffffffffu, need)) {
                 // raise this warp's maxima that need it and rescale their O rows
@@ -264,21 +281,22 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             // P of the tile, once the PV product two tiles back has read the buffer
             if (ok) ok = mbar_wait(&p_empty[sb], ((j >> 1) & 1) ^ 1, err);
-            const float ref = m == -INFINITY ? 0.0f : m;
+            const float nref = m == -INFINITY ? 0.0f : -m;
             uint8_t* prow = prow_base + sb * DT_PBYTES;
+            float2 l2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int c8 = 0; c8 < DT_N / 8; ++c8) {
                 uint32_t w4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t pk = pack_bf16x2(exp2f(__uint_as_float(sr[c8 * 8 + 2 * e]) - ref),
-                                                    exp2f(__uint_as_float(sr[c8 * 8 + 2 * e + 1]) - ref));
-                    const float2 pf = bf16x2_to_f32x2(pk);
-                    l += pf.x + pf.y;
+                    const uint32_t pk = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(sr[c8 * 8 + 2 * e]), sl2, nref)),
+                                                    ex2_approx(fmaf(__uint_as_float(sr[c8 * 8 + 2 * e + 1]), sl2, nref)));
+                    l2 = __fadd2_rn(l2, bf16x2_to_f32x2(pk));
                     w4[e] = pk;
                 }
                 *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
+            l += l2.x + l2.y;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[sb]);
@@ -347,6 +365,7 @@ cudaError_t attention_dense_tc_device_errors(unsigned* bits, bool reset)
 bool attention_dense_tc_supported(const DenseArgs& a)
 {
     if (a.D != DT_D || a.Hq != DT_H || a.L <= 0 || a.L * DT_H > INT32_MAX) return false;
+    if (!(a.softmax_scale > 0.0f)) return false;            // the row maximum is taken on raw scores
     const uintptr_t addr = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
                            reinterpret_cast<uintptr_t>(a.v);
     if (addr & 15) return false;
