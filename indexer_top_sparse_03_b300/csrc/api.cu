@@ -495,18 +495,23 @@ int sparse_attn_prefill(const sa_prefill_args* args, void* ws, size_t ws_bytes, 
         t0 = t1;
     }
     if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
-    // Rows whose history fits in K keep every position, and rows up to 2K keep
-    // at least half of theirs: the dense causal kernel computes them (key tiles
+    // Rows whose history fits in K keep every position, and the next rows keep
+    // a large share of theirs: the dense causal kernel computes them (key tiles
     // shared by 8 queries, rows t >= K masked to their kept positions) more
-    // cheaply than per-row gathers; the gather kernel takes the rest.
+    // cheaply than per-row gathers; the gather kernel takes the rest. A dense
+    // row costs in proportion to t, a gathered one to K; the measured
+    // crossover is at t = 4K on the tensor-core dense kernel (5K the same, 6K
+    // and 3K slower) and at 2K on the mma.sync one.
     const bool aliased = (a.v == a.k) && a.ld_v == a.ld_k;
     int64_t dense_rows = 0;
     if (a.attn_dtype == SA_BF16 && a.dqk == a.dv && !aliased) {
         sa::DenseArgs da{};
         da.q = a.q; da.k = a.k; da.ld_k = a.ld_k; da.v = a.v; da.ld_v = a.ld_v; da.gate = a.gate; da.out = a.out;
-        da.L = 2 * (int64_t)a.K < a.L ? 2 * (int64_t)a.K : a.L; da.Hq = a.Hq; da.D = a.dqk;
+        da.Hq = a.Hq; da.D = a.dqk;
         da.softmax_scale = a.softmax_scale; da.idx = idx; da.K = a.K; da.mask_from = a.K;
-        if (sa::attention_dense_supported(da)) {
+        da.L = 4 * (int64_t)a.K < a.L ? 4 * (int64_t)a.K : a.L;
+        if (!sa::attention_dense_tc_supported(da)) da.L = 2 * (int64_t)a.K < a.L ? 2 * (int64_t)a.K : a.L;
+        if (sa::attention_dense_tc_supported(da) || sa::attention_dense_supported(da)) {
             if (sa::launch_attention_dense(da, stream) != cudaSuccess) return SA_ERR_LAUNCH;
             dense_rows = da.L;
         }

@@ -23,9 +23,8 @@
 //     shared memory as the K-major A operand of the PV product, row sum of
 //     the same rounded values. A row's maximum is raised only when a score
 //     exceeds it by more than 2^8 (then the thread's O row in TMEM and its
-//     sum are rescaled,
-//     which does not change the result); at the end the gate and the bf16
-//     store of the thread's row.
+//     sum are rescaled, which does not change the result); at the end the
+//     gate and the bf16 store of the thread's row.
 #include "attn_common.cuh"
 #include "tc.cuh"
 #include "../../include/sparse_attn.h"

@@ -54,11 +54,12 @@ def _check(cfg, inp, out, idx, rows):
 
 
 def test_rows_of_sixteen_tiles(sa):
-    # rows from 2K on are gathered: K = 2048 kept rows = 16 tiles of 128 keys
-    cfg = get_config("prefill_8k", L=4500)
+    # rows from 4K on are gathered (below, the dense kernel): K = 2048 kept
+    # rows = 16 tiles of 128 keys
+    cfg = get_config("prefill_8k", L=8600)
     inp = make_prefill(cfg, seed=31)
     out, idx = _run(sa, cfg, inp)
-    _check(cfg, inp, out, idx, np.concatenate([np.arange(4096, 4500), np.arange(4090, 4096), [0, 2047]]))
+    _check(cfg, inp, out, idx, np.concatenate([np.arange(8192, 8600), np.arange(8186, 8192), [0, 2047, 4100]]))
 
 
 def test_two_head_groups(sa):

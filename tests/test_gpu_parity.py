@@ -200,10 +200,11 @@ def _check_prefill_rows(cfg, inp, out, idx, rows):
     ("prefill_8k", dict(L=1500, K=256)),
     ("prefill_128k", dict(L=1300, K=200)),
     ("prefill_8k", dict(L=700, K=1024)),          # K >= n for every row: full causal attention
-    # dense rows below 2K with K not a multiple of the 8-row CTA: CTAs straddle
-    # the start of the masked rows (K) and the end of the dense rows (2K)
+    # dense rows below 4K (2K on the mma.sync dense kernel) with K not a
+    # multiple of the 8-row CTA: CTAs straddle the start of the masked rows
+    # (K) and the end of the dense rows
     ("prefill_8k", dict(L=333, K=200)),           # every row on the dense kernel, rows >= 200 masked
-    ("prefill_8k", dict(L=1100, K=257)),          # dense rows 0..513, gathered rows 514..1099
+    ("prefill_8k", dict(L=1100, K=257)),          # dense rows 0..1027, gathered rows 1028..1099
 ])
 def test_prefill_parity(sa, name, over):
     cfg = get_config(name, **over)
