@@ -7,24 +7,30 @@
 // candidate set). dqk = dv = 128, bf16, 16 query heads sharing one key/value
 // head.
 //
-// One CTA per 8 consecutive queries: their 8 x 16 (query, head) rows are the
-// M = 128 side of the MMAs, so a softmax thread owns one whole row of S and
-// of O (TMEM lane = row), and the row's running maximum and sum stay in its
-// registers. CTAs are issued from the last queries down (longest rows first).
-//   - warp 0: TMA loads of the CTA's Q tile (once) and of 64-key K and V
-//     tiles (128-byte swizzle) through a 3-stage ring;
-//   - warp 1 (one thread): S = Q K^T (M = 128, N = 64 keys) into one of two
-//     TMEM buffers, and O += P V (M = 128, N = 128 value columns, the value
-//     tile read MN-major) into a TMEM accumulator; S of tile j + 1 is
-//     computed while the softmax of tile j runs;
-//   - warps 2..5: the softmax, one TMEM lane quarter each: scale to the exp2
-//     domain, causal mask (and, for rows t >= mask_from, the kept-position
-//     bitmap), row maximum, P = exp2(s - m) (the ex2.approx unit) in bf16 to
-//     shared memory as the K-major A operand of the PV product, row sum of
-//     the same rounded values. A row's maximum is raised only when a score
-//     exceeds it by more than 2^8 (then the thread's O row in TMEM and its
-//     sum are rescaled, which does not change the result); at the end the
-//     gate and the bf16 store of the thread's row.
+// One CTA per 16 consecutive queries, as two Q tiles of 8 queries: a tile's
+// 8 x 16 (query, head) rows are the M = 128 side of its MMAs, so a softmax
+// thread owns one whole row of S and of O (TMEM lane = row), and the row's
+// running maximum and sum stay in its registers. CTAs are issued from the
+// last queries down (longest rows first).
+//   - warp 0: TMA loads of the two Q tiles (once) and of 64-key K and V
+//     tiles (128-byte swizzle) through a 3-stage ring; both Q tiles use each
+//     K/V tile;
+//   - warp 1 (one thread): per key tile, S = Q K^T (M = 128, N = 64 keys) of
+//     each Q tile into one of its two TMEM buffers, then O += P V (M = 128,
+//     N = 128 value columns, the value tile read MN-major) of the previous
+//     key tile into each Q tile's TMEM accumulator (the two tiles use all
+//     512 TMEM columns);
+//   - warps 2..5 and 6..9: the softmax of Q tile 0 and of Q tile 1, one TMEM
+//     lane quarter per warp, the two warpgroups running side by side (one
+//     warp per sub-partition was too few to hide the softmax's latencies:
+//     631 -> 674 TFLOP/s at 16K): scale to the exp2 domain, causal mask
+//     (and, for rows t >= mask_from, the kept-position bitmap), row maximum,
+//     P = exp2(s - m) (the ex2.approx unit) in bf16 to shared memory as the
+//     K-major A operand of the PV product, row sum of the same rounded
+//     values. A row's maximum is raised only when a score exceeds it by more
+//     than 2^8 (then the thread's O row in TMEM and its sum are rescaled,
+//     which does not change the result); at the end the gate and the bf16
+//     store of the thread's row.
 #include "attn_common.cuh"
 #include "tc.cuh"
 #include "../../include/sparse_attn.h"
@@ -36,28 +42,32 @@ __device__ unsigned g_dense_tc_error = 0;
 namespace {
 
 constexpr int DT_D = 128;
-constexpr int DT_Q = 8;                        // queries per CTA
+constexpr int DT_Q = 8;                        // queries per Q tile
 constexpr int DT_H = 16;                       // heads per query (one key/value head)
-constexpr int DT_M = DT_Q * DT_H;              // 128 MMA rows
+constexpr int DT_M = DT_Q * DT_H;              // 128 MMA rows per Q tile
+constexpr int DT_G = 2;                        // Q tiles per CTA, each with its own softmax warpgroup
+constexpr int DT_CQ = DT_G * DT_Q;             // queries per CTA
 constexpr int DT_N = 64;                       // keys per tile
 constexpr int DT_STAGES = 3;
-constexpr int DT_QCB = DT_M * 128;             // a 64-column block of the Q tile: 128 rows x 128 B
-constexpr int DT_QBYTES = 2 * DT_QCB;          // 32 KB
+constexpr int DT_QCB = DT_M * 128;             // a 64-column block of a Q tile: 128 rows x 128 B
+constexpr int DT_QBYTES = 2 * DT_QCB;          // 32 KB per Q tile
 constexpr int DT_KCB = DT_N * 128;             // a 64-column block of a key / value tile: 64 rows x 128 B
 constexpr int DT_KV = 2 * DT_KCB;              // 16 KB
 constexpr int DT_STAGE = 2 * DT_KV;            // key tile + value tile
 constexpr int DT_PBYTES = DT_M * 128;          // P tile: 128 rows x 64 keys bf16
-constexpr int DT_OFF_Q = 0;
-constexpr int DT_OFF_KV = DT_OFF_Q + DT_QBYTES;
-constexpr int DT_OFF_P = DT_OFF_KV + DT_STAGES * DT_STAGE;   // [2]
-constexpr int DT_OFF_BAR = DT_OFF_P + 2 * DT_PBYTES;
-constexpr int DT_NBAR = 2 * DT_STAGES + 1 + 2 * 2 + 2 * 2 + 1 + 1;   // kv, q, s, p, o, drain
-constexpr int DT_OFF_BM = DT_OFF_BAR + DT_NBAR * 8 + 16;    // [DT_Q][words] kept-position bitmaps
-constexpr int DT_THREADS = 6 * 32;
-constexpr int DT_EPI = 128;
-constexpr uint32_t DT_TMEM_COLS = 256;        // S [2] x 64 columns, O 128 columns
+constexpr int DT_OFF_Q = 0;                                      // [G]
+constexpr int DT_OFF_KV = DT_OFF_Q + DT_G * DT_QBYTES;           // [STAGES]
+constexpr int DT_OFF_P = DT_OFF_KV + DT_STAGES * DT_STAGE;       // [G] (one P tile per group)
+constexpr int DT_OFF_BAR = DT_OFF_P + DT_G * DT_PBYTES;
+constexpr int DT_GBAR = 2 * 2 + 3;                               // per group: s full + empty [2], p full, p empty, o full
+constexpr int DT_NBAR = 2 * DT_STAGES + 1 + DT_G * DT_GBAR + 1;  // kv, q, groups, drain
+constexpr int DT_OFF_BM = DT_OFF_BAR + DT_NBAR * 8 + 16;         // [CQ][words] kept-position bitmaps
+constexpr int DT_SOFT = 4 * 32;                                  // softmax threads per group
+constexpr int DT_THREADS = (2 + 4 * DT_G) * 32;
+constexpr uint32_t DT_TMEM_COLS = 512;        // per group: S [2] x 64 columns, O 128 columns
 constexpr float DT_RESCALE = 8.0f;
 static_assert(DT_OFF_KV % 1024 == 0 && DT_OFF_P % 1024 == 0 && DT_STAGE % 1024 == 0, "1024-byte tiles");
+static_assert(DT_G * 256 <= (int)DT_TMEM_COLS, "TMEM per group");
 
 constexpr uint32_t DT_IDESC_QK = mma_idesc(1u, DT_M, DT_N);                          // A = Q, B = K (K-major)
 constexpr uint32_t DT_IDESC_PV = mma_idesc(1u, DT_M, DT_D, false, /*b_mn=*/true);    // A = P, B = V (MN-major)
@@ -70,11 +80,11 @@ SA_DEVINL float ex2_approx(float x)
     return y;
 }
 
-SA_DEVINL void bar_soft() { asm volatile("bar.sync 1, %0;" :: "r"(DT_EPI) : "memory"); }
+SA_DEVINL void bar_soft() { asm volatile("bar.sync 1, %0;" :: "r"(DT_G * DT_SOFT) : "memory"); }
 
 __host__ __device__ inline int64_t dt_words(const DenseArgs& a) { return a.idx ? (a.L + 31) / 32 : 0; }
 
-size_t dt_smem(const DenseArgs& a) { return (size_t)DT_OFF_BM + (size_t)DT_Q * dt_words(a) * 4 + 1024; }
+size_t dt_smem(const DenseArgs& a) { return (size_t)DT_OFF_BM + (size_t)DT_CQ * dt_words(a) * 4 + 1024; }
 
 __global__ void __launch_bounds__(DT_THREADS, 1)
 attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -83,32 +93,36 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + DT_OFF_BAR);   // [STAGES] tile landed
-    uint64_t* kv_empty = kv_full + DT_STAGES;                            // [STAGES] PV of the tile done
+    uint64_t* kv_empty = kv_full + DT_STAGES;                            // [STAGES] both PV products done
     uint64_t* q_full = kv_empty + DT_STAGES;
-    uint64_t* s_full = q_full + 1;                                       // [2]
-    uint64_t* s_empty = s_full + 2;                                      // [2]
-    uint64_t* p_full = s_empty + 2;                                      // [2]
-    uint64_t* p_empty = p_full + 2;                                      // [2] PV of that P done
-    uint64_t* o_full = p_empty + 2;
-    uint64_t* drain = o_full + 1;
+    uint64_t* gbar = q_full + 1;                                         // [G][GBAR]
+    uint64_t* drain = gbar + DT_G * DT_GBAR;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     uint32_t* abort_flag = tmem_slot + 1;
-    uint32_t* bm = reinterpret_cast<uint32_t*>(smem + DT_OFF_BM);       // [DT_Q][words]
+    uint32_t* bm = reinterpret_cast<uint32_t*>(smem + DT_OFF_BM);       // [CQ][words]
+    // per group g: s_full [2], s_empty [2], p_full, p_empty (the PV product of the
+    // P tile done: one phase per key tile), o_full
+    auto s_full = [&](int g, int b) { return gbar + g * DT_GBAR + b; };
+    auto s_empty = [&](int g, int b) { return gbar + g * DT_GBAR + 2 + b; };
+    auto p_full = [&](int g) { return gbar + g * DT_GBAR + 4; };
+    auto p_empty = [&](int g) { return gbar + g * DT_GBAR + 5; };
+    auto o_full = [&](int g) { return gbar + g * DT_GBAR + 6; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t0 = (int64_t)(gridDim.x - 1 - blockIdx.x) * DT_Q;
-    const int64_t t_last = min64(t0 + DT_Q, a.L) - 1;
+    const int64_t t0 = (int64_t)(gridDim.x - 1 - blockIdx.x) * DT_CQ;
+    const int64_t t_last = min64(t0 + DT_CQ, a.L) - 1;
     const int ntiles = (int)((t_last + DT_N) / DT_N);                   // keys 0 .. t_last
     unsigned* err = &g_dense_tc_error;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < DT_STAGES; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4); mbar_init(&p_empty[i], 1);
+        for (int g = 0; g < DT_G; ++g) {
+            for (int b = 0; b < 2; ++b) { mbar_init(s_full(g, b), 1); mbar_init(s_empty(g, b), 4); }
+            mbar_init(p_full(g), 4);
+            mbar_init(p_empty(g), 1);
+            mbar_init(o_full(g), 1);
         }
-        mbar_init(o_full, 1);
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -127,9 +141,12 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // ---------------------------------------------------------------- TMA loads
         if (lane == 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(q_full, DT_QBYTES);
-            tma_load_2d(smem + DT_OFF_Q, &tm_q, 0, (int)(t0 * DT_H), q_full);
-            tma_load_2d(smem + DT_OFF_Q + DT_QCB, &tm_q, 64, (int)(t0 * DT_H), q_full);
+            mbar_arrive_expect_tx(q_full, DT_G * DT_QBYTES);
+            for (int g = 0; g < DT_G; ++g) {
+                const int y = (int)((t0 + g * DT_Q) * DT_H);
+                tma_load_2d(smem + DT_OFF_Q + g * DT_QBYTES, &tm_q, 0, y, q_full);
+                tma_load_2d(smem + DT_OFF_Q + g * DT_QBYTES + DT_QCB, &tm_q, 64, y, q_full);
+            }
             for (int kt = 0; kt < ntiles && ok; ++kt) {
                 const int st = kt % DT_STAGES;
                 ok = mbar_wait(&kv_empty[st], ((kt / DT_STAGES) & 1) ^ 1, err);
@@ -150,64 +167,73 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (lane == 0) {
             bool ok = mbar_wait(q_full, 0, err);
             tc_fence_after();
-            const uint32_t qa = smem_u32(smem + DT_OFF_Q);
-            const uint32_t o_t = tmem + 128u;
             for (int j = 0; ok && j <= ntiles; ++j) {
-                if (j < ntiles) {                    // S = Q K^T of tile j
+                if (j < ntiles) {                    // S = Q K^T of tile j, both Q tiles
                     const int st = j % DT_STAGES, sb = j & 1;
-                    ok = mbar_wait(&kv_full[st], (j / DT_STAGES) & 1, err) &&
-                         mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, err);
-                    if (!ok) break;
-                    tc_fence_after();
+                    ok = mbar_wait(&kv_full[st], (j / DT_STAGES) & 1, err);
                     const uint32_t ka = smem_u32(smem + DT_OFF_KV + st * DT_STAGE);
+                    for (int g = 0; ok && g < DT_G; ++g) {
+                        ok = mbar_wait(s_empty(g, sb), ((j >> 1) & 1) ^ 1, err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(smem + DT_OFF_Q + g * DT_QBYTES);
 #pragma unroll
-                    for (int ks = 0; ks < DT_D / 16; ++ks) {
-                        const uint64_t ad = smem_desc_kmajor(qa + (ks >> 2) * DT_QCB + (ks & 3) * 32, 128);
-                        const uint64_t bd = smem_desc_kmajor(ka + (ks >> 2) * DT_KCB + (ks & 3) * 32, 128);
-                        tc_mma_f16(tmem + (uint32_t)(sb * DT_N), ad, bd, DT_IDESC_QK, ks > 0);
+                        for (int ks = 0; ks < DT_D / 16; ++ks) {
+                            const uint64_t ad = smem_desc_kmajor(qa + (ks >> 2) * DT_QCB + (ks & 3) * 32, 128);
+                            const uint64_t bd = smem_desc_kmajor(ka + (ks >> 2) * DT_KCB + (ks & 3) * 32, 128);
+                            tc_mma_f16(tmem + (uint32_t)(g * 256 + sb * DT_N), ad, bd, DT_IDESC_QK, ks > 0);
+                        }
+                        tc_commit(s_full(g, sb));
                     }
-                    tc_commit(&s_full[sb]);
-                }
-                if (j > 0) {                         // O += P V of tile j - 1
-                    const int jp = j - 1, st = jp % DT_STAGES, pb = jp & 1;
-                    ok = mbar_wait(&p_full[pb], (jp >> 1) & 1, err);
                     if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t pa = smem_u32(smem + DT_OFF_P + pb * DT_PBYTES);
+                }
+                if (j > 0) {                         // O += P V of tile j - 1, both Q tiles
+                    const int jp = j - 1, st = jp % DT_STAGES;
                     const uint32_t va = smem_u32(smem + DT_OFF_KV + st * DT_STAGE + DT_KV);
+                    for (int g = 0; ok && g < DT_G; ++g) {
+                        ok = mbar_wait(p_full(g), jp & 1, err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t pa = smem_u32(smem + DT_OFF_P + g * DT_PBYTES);
 #pragma unroll
-                    for (int ks = 0; ks < DT_N / 16; ++ks) {
-                        const uint64_t ad = smem_desc_kmajor(pa + ks * 32, 128);
-                        const uint64_t bd = smem_desc_mnmajor128(va + ks * 2048, DT_KCB, 1024);
-                        tc_mma_f16(o_t, ad, bd, DT_IDESC_PV, (jp > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < DT_N / 16; ++ks) {
+                            const uint64_t ad = smem_desc_kmajor(pa + ks * 32, 128);
+                            const uint64_t bd = smem_desc_mnmajor128(va + ks * 2048, DT_KCB, 1024);
+                            tc_mma_f16(tmem + (uint32_t)(g * 256 + 128), ad, bd, DT_IDESC_PV,
+                                       (jp > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        tc_commit(p_empty(g));
+                        if (j == ntiles) tc_commit(o_full(g));
                     }
+                    if (!ok) break;
                     tc_commit(&kv_empty[st]);
-                    tc_commit(&p_empty[pb]);
-                    if (j == ntiles) tc_commit(o_full);
                 }
             }
             if (!ok) *abort_flag = 1u;
         }
     } else {
         // ---------------------------------------------------------------- softmax and output
+        const int g = (warp - 2) >> 2;                             // Q tile of this warpgroup
         const int q4 = warp & 3;                                   // TMEM lane quarter of this warp
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int r = q4 * 32 + lane;                              // row: query t0 + r / 16, head r % 16
-        const int qi = r / DT_H, h = r % DT_H;
+        const uint32_t s_t = tmem + lane_off + (uint32_t)(g * 256);
+        const uint32_t o_t = s_t + 128u;
+        const int r = q4 * 32 + lane;                              // row: query r / 16 of the tile, head r % 16
+        const int qi = g * DT_Q + r / DT_H, h = r % DT_H;
         const int64_t t = t0 + qi;
         const float sl2 = a.softmax_scale * LOG2E;
         const int64_t words = dt_words(a);
         // kept-position bitmaps of the CTA's masked queries (rows t >= mask_from)
         const bool masked = a.idx != nullptr && t >= a.mask_from && t < a.L;
         if (a.idx) {
-            const int et = threadIdx.x - 64;                       // 0 .. 127
-            for (int64_t i = et; i < DT_Q * words; i += DT_EPI) bm[i] = 0u;
+            const int et = threadIdx.x - 64;                       // 0 .. G * 128 - 1
+            for (int64_t i = et; i < DT_CQ * words; i += DT_G * DT_SOFT) bm[i] = 0u;
             bar_soft();
-            for (int qq = 0; qq < DT_Q; ++qq) {
+            for (int qq = 0; qq < DT_CQ; ++qq) {
                 const int64_t tq = t0 + qq;
                 if (tq >= a.L || tq < a.mask_from) continue;
                 const int32_t* sel = a.idx + tq * a.K;
-                for (int i = et; i < a.K; i += DT_EPI) {
+                for (int i = et; i < a.K; i += DT_G * DT_SOFT) {
                     const int32_t p = sel[i];
                     if (p >= 0 && p <= tq) atomicOr(&bm[qq * words + (p >> 5)], 1u << (p & 31));
                 }
@@ -215,20 +241,20 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bar_soft();
         }
         const uint32_t* mybm = bm + qi * words;
-        uint8_t* prow_base = smem + DT_OFF_P + r * 128;
+        uint8_t* prow = smem + DT_OFF_P + g * DT_PBYTES + r * 128;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int sb = j & 1;
-            if (ok) ok = mbar_wait(&s_full[sb], (j >> 1) & 1, err);
+            if (ok) ok = mbar_wait(s_full(g, sb), (j >> 1) & 1, err);
             tc_fence_after();
             uint32_t sr[DT_N];
-            tmem_ld32(tmem + lane_off + (uint32_t)(sb * DT_N), *reinterpret_cast<uint32_t(*)[32]>(sr));
-            tmem_ld32(tmem + lane_off + (uint32_t)(sb * DT_N + 32), *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_ld32(s_t + (uint32_t)(sb * DT_N), *reinterpret_cast<uint32_t(*)[32]>(sr));
+            tmem_ld32(s_t + (uint32_t)(sb * DT_N + 32), *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[sb]);
+            if (lane == 0) mbar_arrive(s_empty(g, sb));
             // keys j0 .. j0 + 63: causal (<= t) and, for masked rows, kept
             const int64_t j0 = (int64_t)j * DT_N;
             uint64_t keep = ~0ull;
@@ -263,25 +289,24 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     l *= f;
                 }
                 if (j > 0) {
-                    if (ok) ok = mbar_wait(&p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, err);
+                    if (ok) ok = mbar_wait(p_empty(g), (j - 1) & 1, err);
                     tc_fence_after();
 #pragma unroll
                     for (int c0 = 0; c0 < DT_D; c0 += 32) {
                         uint32_t o[32];
-                        tmem_ld32(tmem + lane_off + 128u + (uint32_t)c0, o);
+                        tmem_ld32(o_t + (uint32_t)c0, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
-                        tmem_st32(tmem + lane_off + 128u + (uint32_t)c0, o);
+                        tmem_st32(o_t + (uint32_t)c0, o);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                 }
             }
-            // P of the tile, once the PV product two tiles back has read the buffer
-            if (ok) ok = mbar_wait(&p_empty[sb], ((j >> 1) & 1) ^ 1, err);
+            // P of the tile, once the PV product of the previous tile has read the buffer
+            if (ok) ok = mbar_wait(p_empty(g), (j & 1) ^ 1, err);
             const float nref = m == -INFINITY ? 0.0f : -m;
-            uint8_t* prow = prow_base + sb * DT_PBYTES;
             float2 l2 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int c8 = 0; c8 < DT_N / 8; ++c8) {
@@ -298,17 +323,17 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             l += l2.x + l2.y;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
+            if (lane == 0) mbar_arrive(p_full(g));
         }
         // the row's output
-        if (ok) ok = mbar_wait(o_full, 0, err);
+        if (ok) ok = mbar_wait(o_full(g), 0, err);
         tc_fence_after();
         const float gs = (t < a.L && l > 0.0f) ? (1.0f / (1.0f + expf(-a.gate[t * a.Hq + h]))) / l : 0.0f;
         bf16* out = static_cast<bf16*>(a.out) + (t * a.Hq + h) * DT_D;
 #pragma unroll
         for (int c0 = 0; c0 < DT_D; c0 += 32) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + 128u + (uint32_t)c0, o);
+            tmem_ld32(o_t + (uint32_t)c0, o);
             tmem_ld_wait();
             if (t < a.L) {
 #pragma unroll
@@ -387,7 +412,7 @@ cudaError_t launch_attention_dense_tc(const DenseArgs& a, cudaStream_t s)
         (void)cudaGetLastError();
         return e;
     }
-    const unsigned grid = (unsigned)((a.L + DT_Q - 1) / DT_Q);
+    const unsigned grid = (unsigned)((a.L + DT_CQ - 1) / DT_CQ);
     return launch_kernel(attn_dense_tc_kernel, dim3(grid), dim3(DT_THREADS), smem, s, false, tq, tk, tv, a);
 }
 
