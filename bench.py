@@ -447,8 +447,13 @@ def bench_variants(sa, torch, dev, seed, iters=5):
         ms = timed(lambda: sa.sparse_attn_prefill_local(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"],
                                                         inp["w"], inp["gate"], cfg.K, scale, win, out=out))
         res[f"local_{win}"] = {"workload": cfg.name, "window": win, "K": cfg.K, "ms": ms, "tok_s": cfg.L / (ms * 1e-3)}
-    # the attention stage (dense rows below 2K + gathered rows) under each
-    # kernel choice for the gathered rows
+    # the attention stage under each kernel choice for the gathered rows, at
+    # the 8K prefill's shapes and L = 16384 (rows below 4K = 8192 go to the
+    # dense kernel whatever the choice, the other half is gathered)
+    del out, inp
+    cfg = get_config(PREFILL_WORKLOAD, L=16384)
+    inp = make_prefill(cfg, seed=seed, device=dev)
+    out = torch.empty((cfg.L, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     kernels = {}
     for name, which in (("mma_sync", sa.ATTN_AUTO), ("tcgen05", sa.ATTN_TCGEN05)):
@@ -464,11 +469,11 @@ def bench_variants(sa, torch, dev, seed, iters=5):
         finally:
             sa.set_prefill_attention_kernel(prev)
         kernels[name] = statistics.median(times[1:])
-    res["prefill_attention_kernels"] = {"workload": cfg.name, "attention_ms": kernels}
+    res["prefill_attention_kernels"] = {"workload": cfg.name, "L": cfg.L, "attention_ms": kernels}
     return res
 
 
-def bench_break_even(sa, torch, dev, seed, lengths=(4096, 8192, 16384, 32768), iters=3):
+def bench_break_even(sa, torch, dev, seed, lengths=(4096, 8192, 16384, 32768, 65536), iters=3):
     """Full attention against the sparse layer across lengths, at the 8K
     prefill's shapes (K = 2048): dense causal attention time, and the sparse
     prefill split into selection (indexer + Top-K) and sparse attention;
