@@ -602,15 +602,36 @@ int sparse_attn_prefill_blocks(const sa_prefill_args* args, int block_size, void
             return SA_ERR_LAUNCH;
     }
     if (a.stage_events && cudaEventRecord(a.stage_events[0], stream) != cudaSuccess) return SA_ERR_LAUNCH;
-    sa::AttnArgs at{};
-    at.q = a.q; at.k = a.k; at.ld_k = a.ld_k; at.v = a.v; at.ld_v = a.ld_v;
-    at.v_aliases_k = (a.v == a.k) && a.ld_v == a.ld_k;
-    at.row_base = nullptr; at.idx = idx; at.K = a.K; at.ctx_len = nullptr; at.kept_len = cnt;
-    at.causal_first = 0; at.n_cap = a.L; at.gate = a.gate;
-    at.rows = a.L; at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
-    at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype; at.out = a.out;
-    at.splits = 1; at.part = nullptr; at.tickets = nullptr;
-    if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    // as in the token-level prefill, the rows below 4K go through the
+    // tensor-core dense kernel masked to their kept positions (every row:
+    // the expanded block lists are -1 padded like the token lists)
+    const bool aliased = (a.v == a.k) && a.ld_v == a.ld_k;
+    int64_t dense_rows = 0;
+    if (a.attn_dtype == SA_BF16 && a.dqk == a.dv && !aliased) {
+        sa::DenseArgs da{};
+        da.q = a.q; da.k = a.k; da.ld_k = a.ld_k; da.v = a.v; da.ld_v = a.ld_v; da.gate = a.gate; da.out = a.out;
+        da.Hq = a.Hq; da.D = a.dqk; da.softmax_scale = a.softmax_scale; da.idx = idx; da.K = a.K; da.mask_from = 0;
+        da.L = 4 * (int64_t)a.K < a.L ? 4 * (int64_t)a.K : a.L;
+        if (sa::attention_dense_tc_supported(da)) {
+            if (sa::launch_attention_dense(da, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+            dense_rows = da.L;
+        }
+    }
+    if (dense_rows < a.L) {
+        const size_t es = a.attn_dtype == SA_BF16 ? 2 : 4;
+        sa::AttnArgs at{};
+        at.q = static_cast<const char*>(a.q) + (size_t)dense_rows * a.Hq * a.dqk * es;
+        at.k = a.k; at.ld_k = a.ld_k; at.v = a.v; at.ld_v = a.ld_v;
+        at.v_aliases_k = aliased;
+        at.row_base = nullptr; at.idx = idx + dense_rows * a.K; at.K = a.K; at.ctx_len = nullptr;
+        at.kept_len = cnt + dense_rows;
+        at.causal_first = dense_rows; at.n_cap = a.L; at.gate = a.gate + dense_rows * a.Hq;
+        at.rows = (int)(a.L - dense_rows); at.Hq = a.Hq; at.dqk = a.dqk; at.dv = a.dv;
+        at.softmax_scale = a.softmax_scale; at.dtype = a.attn_dtype;
+        at.out = static_cast<char*>(a.out) + (size_t)dense_rows * a.Hq * a.dv * es;
+        at.splits = 1; at.part = nullptr; at.tickets = nullptr;
+        if (sa::launch_attention(at, stream) != cudaSuccess) return SA_ERR_LAUNCH;
+    }
     if (a.stage_events && cudaEventRecord(a.stage_events[1], stream) != cudaSuccess) return SA_ERR_LAUNCH;
     return SA_OK;
 }
