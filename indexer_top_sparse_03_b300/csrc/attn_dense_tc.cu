@@ -80,6 +80,13 @@ SA_DEVINL float ex2_approx(float x)
     return y;
 }
 
+SA_DEVINL float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 SA_DEVINL void bar_soft() { asm volatile("bar.sync 1, %0;" :: "r"(DT_G * DT_SOFT) : "memory"); }
 
 __host__ __device__ inline int64_t dt_words(const DenseArgs& a) { return a.idx ? (a.L + 31) / 32 : 0; }
@@ -265,19 +272,20 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (t >= a.L) keep = 0ull;
             // the row maximum on the raw scores (the scale is positive); masked
             // keys become -inf, which the exponential below maps to 0
-            float tmax = -INFINITY;
-            if (__all_sync(0xffffffffu, keep == ~0ull)) {
+            if (!__all_sync(0xffffffffu, keep == ~0ull)) {
 #pragma unroll
-                for (int c = 0; c < DT_N; ++c) tmax = fmaxf(tmax, __uint_as_float(sr[c]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < DT_N; ++c) {
-                    const float x = ((keep >> c) & 1ull) ? __uint_as_float(sr[c]) : -INFINITY;
-                    sr[c] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
-                }
+                for (int c = 0; c < DT_N; ++c)
+                    if (!((keep >> c) & 1ull)) sr[c] = __float_as_uint(-INFINITY);
             }
-            tmax *= sl2;
+            // four independent chains of three-input maxima (not one 64-deep chain)
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < DT_N; c += 8) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mx[u] = fmax3(mx[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
+            }
+            float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
             const bool need = tmax > m + DT_RESCALE;
             if (__any_sync(0xffffffffu, need)) {
                 // raise this warp's maxima that need it and rescale their O rows
@@ -307,7 +315,8 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             // P of the tile, once the PV product of the previous tile has read the buffer
             if (ok) ok = mbar_wait(p_empty(g), (j & 1) ^ 1, err);
             const float nref = m == -INFINITY ? 0.0f : -m;
-            float2 l2 = make_float2(0.0f, 0.0f);
+            float2 l2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                            make_float2(0.0f, 0.0f)};
 #pragma unroll
             for (int c8 = 0; c8 < DT_N / 8; ++c8) {
                 uint32_t w4[4];
@@ -315,12 +324,12 @@ attn_dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 for (int e = 0; e < 4; ++e) {
                     const uint32_t pk = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(sr[c8 * 8 + 2 * e]), sl2, nref)),
                                                     ex2_approx(fmaf(__uint_as_float(sr[c8 * 8 + 2 * e + 1]), sl2, nref)));
-                    l2 = __fadd2_rn(l2, bf16x2_to_f32x2(pk));
+                    l2[e] = __fadd2_rn(l2[e], bf16x2_to_f32x2(pk));
                     w4[e] = pk;
                 }
                 *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            l += l2.x + l2.y;
+            l += ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(g));
