@@ -324,7 +324,7 @@ def indexer_roofline(sa, torch, dev, cfg, inp, iters):
     del scores
     return {"kernel": "indexer_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
-            "peak_source": peaks["source"] + " burst bf16 (the north-star reference for both dtypes)",
+            "peak_source": peaks["source"] + " burst bf16 (the reference for both dtypes: the target is stated against bf16)",
             "algorithmic_flops": flops, "ms": ms, "dtype": str(inp["q_idx"].dtype).replace("torch.", "")}
 
 
