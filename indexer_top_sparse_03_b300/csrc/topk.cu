@@ -204,7 +204,7 @@ topk_rows_kernel(TopkArgs a)
         uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem);
         for (int64_t j = tid; j < n; j += TK_THREADS) keys[j] = score_key(row[j]);
         __syncthreads();
-        radix_select_row([&](int64_t j) { return keys[j]; }, n, K, out, sh);
+        radix_select_row([&](int64_t j) { return keys[j]; }, n, K, out, sh, keys);
         return;
     }
     unsigned* hist = reinterpret_cast<unsigned*>(tk_smem);
@@ -262,7 +262,7 @@ topk_short_kernel(TopkArgs a)
         atomicAdd(&sh.hist[k >> 24], 1u);
     }
     __syncthreads();
-    radix_select_row<true>([&](int64_t j) { return keys[j]; }, n, K, out, sh);
+    radix_select_row<true>([&](int64_t j) { return keys[j]; }, n, K, out, sh, keys);
 }
 
 constexpr int TK_SHORT_THREADS = 128;

@@ -241,8 +241,12 @@ SA_DEVINL uint32_t block_max_u32(uint32_t v, unsigned* warp_tot)
 // multiple of 32.
 // With HIST0 the caller has already counted the top digits (key >> 24) of
 // all n keys into sh.hist (and synchronised), so the first pass is skipped.
+// `staged`, when given, holds the same n keys in 16-byte-aligned shared
+// memory: the counting passes (which do not depend on the order of the keys)
+// then read four keys per load.
 template <bool HIST0 = false, typename KeyAt>
-__device__ void radix_select_row(KeyAt key_at, int64_t n, int K, int32_t* out, RadixShared& sh)
+__device__ void radix_select_row(KeyAt key_at, int64_t n, int K, int32_t* out, RadixShared& sh,
+                                 const uint32_t* staged = nullptr)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nth = blockDim.x;
     uint32_t prefix = 0, mask = 0;
@@ -251,10 +255,20 @@ __device__ void radix_select_row(KeyAt key_at, int64_t n, int K, int32_t* out, R
         if (!HIST0 || shift != 24) {
             for (int i = tid; i < RADIX; i += nth) sh.hist[i] = 0;
             __syncthreads();
-            for (int64_t j = tid; j < n; j += nth) {
-                const uint32_t u = key_at(j);
+            auto count = [&](uint32_t u) {
                 if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & (RADIX - 1)], 1u);
+            };
+            int64_t j_tail = 0;
+            if (staged) {                    // 16-byte-aligned keys in shared memory: four per load
+                const int64_t n4 = n >> 2;
+                const uint4* s4 = reinterpret_cast<const uint4*>(staged);
+                for (int64_t i = tid; i < n4; i += nth) {
+                    const uint4 u = s4[i];
+                    count(u.x); count(u.y); count(u.z); count(u.w);
+                }
+                j_tail = n4 << 2;
             }
+            for (int64_t j = j_tail + tid; j < n; j += nth) count(key_at(j));
             __syncthreads();
         }
         if (warp == 0) radix_find_digit(sh, need);
